@@ -1,0 +1,287 @@
+// Shared device-side definitions of the speculative-pipeline-decoding library.
+//
+// Layout of the run state in HBM (all carved out of the caller's workspace):
+//   slot ring     n+1 slots; stage s of the current step lives in slot (head - s) mod (n+1),
+//                 the token that left the last stage in the previous step ("exited row",
+//                 read once more by the draft module) in slot (head - n) mod (n+1).
+//   X   fp32 [n+1][d]            residual stream per slot
+//   ANCH fp32 [n+1][nB][d]       anchor states per slot (depth a = after a layers, 0 = embedding)
+//   QKV fp32 [n][(Hq+2Hkv) hd]   raw q,k,v of each stage (RoPE is applied by the attention kernel)
+//   ATT fp32 [n][Hq hd]          attention output of each stage
+//   U   fp32 [n][F]              silu(gate) * up of each stage
+//   K/V cache per target layer   dtype [max_seq][Hkv][hd]; valid length per layer in DevState
+//   draft module buffers         Xp [n+1][d], QKVp/ATTp/GUp per row, its own K/V cache
+//   logits fp32 [2][V]           row 0 = target prediction of the exiting token, row 1 = draft
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/spd.h"
+
+namespace spd {
+
+constexpr int MAXS = 32;                 // ring slots (n + 1 <= 32)
+constexpr int MAXL = SPD_MAX_LAYERS;
+constexpr int MAXPL = SPD_MAX_PDM_LAYERS;
+constexpr int MAXB = SPD_MAX_ANCHORS;
+constexpr int ATT_CHUNK = 128;           // positions per attention split (fixed: results independent of grouping)
+constexpr int GEMV_THREADS = 256;
+constexpr int GEMV_WARPS = GEMV_THREADS / 32;
+constexpr int SK_ROWS = 128;             // rows per CTA of the draft-module skinny GEMM (8 warps x 16)
+constexpr int SK_KCHUNK = 64;            // K elements per mma iteration (two m16n8k16 steps)
+constexpr int MAX_R = MAXS;              // draft-module rows per step (n+1)
+
+// device error codes (DevState::error)
+constexpr int ERR_FORCED_REF = 1;
+constexpr int ERR_TRACE_FULL = 2;
+constexpr int ERR_SEQ_FULL = 3;
+constexpr int ERR_ROWS = 4;
+constexpr int ERR_TOKEN = 5;
+
+struct LayerW {
+    const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+    const float *g1, *g2;
+};
+
+struct DevState {
+    int head, t, N, done, pending, error, pdm_len, prompt_len;   // first 8: SPD_BUF_STATE
+    int valid[MAXS], pos[MAXS], tok[MAXS];
+    int len[MAXL];
+    // argmax results of the last LM-head pass (row 0 target, row 1 draft)
+    int top[2];
+    float topval[2];
+    // draft distribution normalisers per slot (T > 0): max and sum of exp(z/T - max)
+    float dmax[MAXS], dsum[MAXS];
+    long long accepts, rejects, run_cur, run_sum, run_count;
+    double weight_bytes;
+};
+
+// Constant description of one handle: shapes, stage plan, weight and buffer pointers.
+struct Plan {
+    int L, d, Hq, Hkv, hd, F, V, n, nB, Ls, max_seq, max_new, max_steps, dtype;
+    int qkv_rows, q_rows, kv_rows;
+    int J;                         // rounds per step = longest stage
+    int b[MAXS + 1];               // stage bounds
+    int anchors[MAXB];
+    signed char aidx[MAXL + 1];    // anchor index of depth a, or -1
+    float eps, scale, temperature;
+    unsigned seed_lo, seed_hi;
+    int forced;
+    unsigned forced_thr;           // coin: u24 < forced_thr keeps forced_ref
+    const int *forced_ref;
+    int forced_ref_len;
+    // weights
+    const void *embed, *lm_head, *pdm_lm_head, *proj;
+    const float *gf, *pdm_gf;
+    LayerW tl[MAXL];
+    LayerW pl[MAXPL];
+    // workspace
+    float *X, *QKV, *ATT, *U, *ANCH;
+    void *kc, *vc, *pkc, *pvc;
+    long long kv_stride;           // elements per layer cache
+    float2 *rope;                  // [max_seq][hd/2] (cos, sin)
+    float *att_part, *patt_part;   // [MAXS][Hq][max_chunks][hd + 2] (target / draft module)
+    int *att_cnt, *patt_cnt;       // [MAXS][Hkv]
+    int att_max_chunks;
+    long long layer_bytes;         // weight bytes of one target layer
+    long long pdm_bytes;           // draft module per step (projection + layers)
+    long long lm_bytes;            // LM head per step
+    float *Xp, *QKVp, *ATTp, *GUp, *inv_rms_p;
+    float *sk_part;                // draft skinny GEMM split-K partials
+    int *sk_cnt;                   // per row-block counters + 1 global
+    int sk_max_rowblocks, sk_max_kseg;
+    float *logits;                 // [2][V]
+    float *dlogits;                // [n+1][V] draft logits per slot (T > 0)
+    float *lm_part;                // [grid][2] (val, idx as float bits)
+    int *lm_cnt;
+    DevState *st;
+    spd_trace_rec *trace;
+    int *trace_len;                // [max_steps][L]
+    int *out_tokens;               // [max_new]
+    // prefill scratch
+    int pf_rows;                   // rows per prefill chunk
+    float *pf_H, *pf_XN, *pf_QKV, *pf_ATT, *pf_GU, *pf_ANCH, *pf_Hp;
+    float *pf_logits;              // [V]
+    Plan *self;                    // device address of this plan
+};
+
+// ---------------------------------------------------------------------------------
+// element access
+template <typename T> struct WTraits;
+template <> struct WTraits<float> {
+    static constexpr int VEC = 4;   // elements per 16-byte load
+    __device__ static __forceinline__ float get(const float *p, long long i) { return p[i]; }
+    __device__ static __forceinline__ float store(float v) { return v; }
+};
+template <> struct WTraits<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    __device__ static __forceinline__ float get(const __nv_bfloat16 *p, long long i) { return __bfloat162float(p[i]); }
+    __device__ static __forceinline__ __nv_bfloat16 store(float v) { return __float2bfloat16_rn(v); }
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// Dot product of one 16-byte weight vector with the matching x values (fixed order).
+__device__ __forceinline__ float dot16(const uint4 &w, const float *x, float acc, __nv_bfloat16) {
+    const float4 x0 = *reinterpret_cast<const float4 *>(x);
+    const float4 x1 = *reinterpret_cast<const float4 *>(x + 4);
+    acc = fmaf(bf_lo(w.x), x0.x, acc);
+    acc = fmaf(bf_hi(w.x), x0.y, acc);
+    acc = fmaf(bf_lo(w.y), x0.z, acc);
+    acc = fmaf(bf_hi(w.y), x0.w, acc);
+    acc = fmaf(bf_lo(w.z), x1.x, acc);
+    acc = fmaf(bf_hi(w.z), x1.y, acc);
+    acc = fmaf(bf_lo(w.w), x1.z, acc);
+    acc = fmaf(bf_hi(w.w), x1.w, acc);
+    return acc;
+}
+__device__ __forceinline__ float dot16(const uint4 &w, const float *x, float acc, float) {
+    const float4 x0 = *reinterpret_cast<const float4 *>(x);
+    acc = fmaf(__uint_as_float(w.x), x0.x, acc);
+    acc = fmaf(__uint_as_float(w.y), x0.y, acc);
+    acc = fmaf(__uint_as_float(w.z), x0.z, acc);
+    acc = fmaf(__uint_as_float(w.w), x0.w, acc);
+    return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Block-wide sum with a fixed reduction tree (result broadcast to all threads).
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float s = 0.f;
+    if (w == 0) {
+        s = lane < nw ? red[lane] : 0.f;
+        s = warp_sum(s);
+        if (lane == 0) red[32] = s;
+    }
+    __syncthreads();
+    return red[32];
+}
+__device__ __forceinline__ float block_max(float v, float *red) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float s = -INFINITY;
+    if (w == 0) {
+        s = lane < nw ? red[lane] : -INFINITY;
+        s = warp_max(s);
+        if (lane == 0) red[32] = s;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+__device__ __forceinline__ int ring(int head, int s, int nslots) {
+    int r = (head - s) % nslots;
+    return r < 0 ? r + nslots : r;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Philox4x32-10 (Salmon et al., SC'11): two 32x32->64-bit multiplies per round,
+// Weyl-sequence key schedule, ten rounds.  Counter (t, purpose, 0, 0), key (lo, hi).
+__device__ __forceinline__ uint32_t philox_word0(uint32_t t, uint32_t purpose, uint32_t klo, uint32_t khi) {
+    uint32_t c0 = t, c1 = purpose, c2 = 0u, c3 = 0u;
+    uint32_t k0 = klo, k1 = khi;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return c0;
+}
+
+// Rows of the draft module in the current step: the token that left the pipeline in
+// the previous step (all anchors, cached permanently from now on), then the in-flight
+// tokens oldest first; consecutive positions pos0, pos0+1, ...
+struct PdmRows {
+    int R, pos0;
+    int slot[MAXS], depth[MAXS];
+};
+
+__device__ __forceinline__ void build_pdm_rows(const Plan *__restrict__ P, PdmRows &pr) {
+    const DevState *st = P->st;
+    const int n = P->n, ns = n + 1, head = st->head;
+    int R = 0, pos0 = 0;
+    if (st->pending) {
+        const int slot = ring(head, n, ns);
+        pr.slot[0] = slot;
+        pr.depth[0] = P->L;
+        pos0 = st->pos[slot];
+        R = 1;
+    }
+    for (int s = n - 1; s >= 0; --s) {
+        const int slot = ring(head, s, ns);
+        if (!st->valid[slot]) continue;
+        if (R == 0) pos0 = st->pos[slot];
+        pr.slot[R] = slot;
+        pr.depth[R] = P->b[s];
+        ++R;
+    }
+    pr.R = R;
+    pr.pos0 = pos0;
+}
+
+// ---------------------------------------------------------------------------------
+// launch helpers (defined in the kernel translation units)
+template <typename T> void launch_target_round(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
+template <typename T> void launch_target_qkv(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
+template <typename T> void launch_target_attn(const Plan *P, const Plan &h, int round, cudaStream_t s);
+template <typename T> void launch_target_oproj(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
+template <typename T> void launch_target_gateup(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
+template <typename T> void launch_target_down(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
+template <typename T> void launch_lm_head(const Plan *P, const Plan &h, int grid, cudaStream_t s);
+struct SkPlan { int nks[5]; int smem; int NT; };   // split-K per draft GEMM: proj, qkv, o, gateup, down
+template <typename T> void launch_pdm_step(const Plan *P, const Plan &h, const SkPlan &sk, cudaStream_t s);
+template <typename T> void launch_pdm_attn(const Plan *P, const Plan &h, int layer, cudaStream_t s);
+void sk_plan(const Plan &h, int num_sms, SkPlan &sk);
+void set_pdm_attributes(int smem);
+void set_target_attributes(int smem);
+void set_prefill_attributes();
+template <typename T> void launch_verify(const Plan *P, const Plan &h, cudaStream_t s);
+template <typename T> void launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int grid,
+                                          cudaStream_t s);
+template <typename T> void launch_prefill_finalize(const Plan *P, int prompt_len, cudaStream_t s);
+void launch_rope_table(const Plan &h, float theta, cudaStream_t s);
+int gemv_smem_bytes(const Plan &h);
+int target_blocks_per_sm(int dtype, int smem);
+int lm_blocks_per_sm(int dtype, int smem, bool tied);
+void set_kernel_attributes(int dtype, int gemv_smem);
+
+}  // namespace spd

@@ -1,0 +1,342 @@
+// Prefill: the prompt's dense pass through all target layers, the draft module's cached
+// prefix, and the first token.  Not part of the timed step; it fills what the step
+// needs: every layer's K,V for the prompt positions and the draft module's K,V built
+// from full-depth anchor features of the verified prefix (machine review "What carries
+// the argument": "depth-maximized features for verified prefixes").
+//
+// The prompt is processed in chunks of pf_rows positions (each chunk attends causally to
+// the cache of the chunks before it), with an fp32 tiled CUDA-core GEMM (weights bf16 or
+// fp32) and a tiled causal attention whose K/V tiles are staged in shared memory.
+#include "common.cuh"
+
+namespace spd {
+
+// ---------------------------------------------------------------------------------
+// C[M][N] (+)= A[M][K] * W[N][K]^T ; 128x128 tiles, 8x8 outputs per thread
+constexpr int GM = 128, GN = 128, GK = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_pf_gemm(const float *__restrict__ A, int lda, const T *__restrict__ W, int N,
+                                                int K, float *__restrict__ C, int ldc, int M, int accumulate) {
+    __shared__ __align__(16) float As[GK][GM + 4];
+    __shared__ __align__(16) float Ws[GK][GN + 4];
+    const int t = threadIdx.x;
+    const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
+    const int ty = t / 16, tx = t % 16;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    const int lr = t / 2, lk = (t % 2) * 4;
+    for (int k0 = 0; k0 < K; k0 += GK) {
+        {
+            const int m = m0 + lr;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (m < M) v = *reinterpret_cast<const float4 *>(A + (long long)m * lda + k0 + lk);
+            As[lk + 0][lr] = v.x;
+            As[lk + 1][lr] = v.y;
+            As[lk + 2][lr] = v.z;
+            As[lk + 3][lr] = v.w;
+            const int n = n0 + lr;
+            float w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;
+            if (n < N) {
+                const T *wp = W + (long long)n * K + k0 + lk;
+                w0 = WTraits<T>::get(wp, 0);
+                w1 = WTraits<T>::get(wp, 1);
+                w2 = WTraits<T>::get(wp, 2);
+                w3 = WTraits<T>::get(wp, 3);
+            }
+            Ws[lk + 0][lr] = w0;
+            Ws[lk + 1][lr] = w1;
+            Ws[lk + 2][lr] = w2;
+            Ws[lk + 3][lr] = w3;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < GK; ++k) {
+            float a[8], w[8];
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[k][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[k][64 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Ws[k][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Ws[k][64 + tx * 4]);
+            a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+            a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+            w[0] = b0.x; w[1] = b0.y; w[2] = b0.z; w[3] = b0.w;
+            w[4] = b1.x; w[5] = b1.y; w[6] = b1.z; w[7] = b1.w;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+        if (m >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+            if (n >= N) continue;
+            float *c = C + (long long)m * ldc + n;
+            *c = accumulate ? *c + acc[i][j] : acc[i][j];
+        }
+    }
+}
+
+template <typename T>
+static void pf_gemm(const float *A, int lda, const void *W, int N, int K, float *C, int ldc, int M, int acc,
+                    cudaStream_t s) {
+    dim3 grid((N + GN - 1) / GN, (M + GM - 1) / GM);
+    k_pf_gemm<T><<<grid, 256, 0, s>>>(A, lda, reinterpret_cast<const T *>(W), N, K, C, ldc, M, acc);
+}
+
+// ---------------------------------------------------------------------------------
+template <typename T>
+__global__ void k_pf_embed(const Plan *__restrict__ P, const int *__restrict__ prompt, int p0) {
+    const int m = blockIdx.x, d = P->d;
+    int tok = prompt[p0 + m];
+    if (tok < 0 || tok >= P->V) {
+        if (threadIdx.x == 0) P->st->error = ERR_TOKEN;
+        tok = 0;
+    }
+    const T *e = reinterpret_cast<const T *>(P->embed) + (long long)tok * d;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) {
+        const float v = WTraits<T>::get(e, k);
+        P->pf_H[(long long)m * d + k] = v;
+        P->pf_ANCH[(long long)m * P->nB * d + k] = v;
+    }
+}
+
+__global__ void k_pf_norm(const float *__restrict__ src, float *__restrict__ dst, const float *__restrict__ g, int d,
+                          float eps) {
+    __shared__ float red[40];
+    const float *x = src + (long long)blockIdx.x * d;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) ss = fmaf(x[k], x[k], ss);
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int k = threadIdx.x; k < d; k += blockDim.x) dst[(long long)blockIdx.x * d + k] = (x[k] * inv) * g[k];
+}
+
+template <typename T>
+__global__ void k_pf_rope_kv(const Plan *__restrict__ P, float *__restrict__ qkv, int p0, T *__restrict__ kc,
+                             T *__restrict__ vc) {
+    const int m = blockIdx.x, pos = p0 + m;
+    const int hd = P->hd, half = hd / 2;
+    float *row = qkv + (long long)m * P->qkv_rows;
+    const float2 *cs = P->rope + (long long)pos * half;
+    const long long rs = (long long)P->Hkv * hd;
+    // q heads (in place)
+    for (int idx = threadIdx.x; idx < P->Hq * half; idx += blockDim.x) {
+        const int h = idx / half, i = idx % half;
+        float *q = row + (long long)h * hd;
+        const float a = q[i], b = q[i + half];
+        const float2 r = cs[i];
+        q[i] = a * r.x - b * r.y;
+        q[i + half] = b * r.x + a * r.y;
+    }
+    for (int idx = threadIdx.x; idx < P->Hkv * half; idx += blockDim.x) {
+        const int h = idx / half, i = idx % half;
+        const float *k = row + P->q_rows + (long long)h * hd;
+        const float a = k[i], b = k[i + half];
+        const float2 r = cs[i];
+        kc[(long long)pos * rs + (long long)h * hd + i] = WTraits<T>::store(a * r.x - b * r.y);
+        kc[(long long)pos * rs + (long long)h * hd + i + half] = WTraits<T>::store(b * r.x + a * r.y);
+    }
+    for (int idx = threadIdx.x; idx < P->kv_rows; idx += blockDim.x)
+        vc[(long long)pos * rs + idx] = WTraits<T>::store(row[P->q_rows + P->kv_rows + idx]);
+}
+
+// Causal attention of M prompt rows (positions p0..p0+M-1) over cache positions
+// 0..p0+M-1.  CTA = (block of QB query rows, kv head); thread = (row, head of the GQA
+// group, quarter of the head dim; dims sub, sub+4, ...).  Online softmax over 64-key
+// tiles staged in shared memory.
+constexpr int PF_KT = 64;
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) k_pf_attn(const Plan *__restrict__ P, const float *__restrict__ qkv, int p0,
+                                                 int M, const T *__restrict__ kc, const T *__restrict__ vc,
+                                                 float *__restrict__ out) {
+    extern __shared__ __align__(16) float kvs[];
+    constexpr int hd = HD, DS = HD / 4;
+    const int G = P->Hq / P->Hkv, Hkv = P->Hkv;
+    const int QB = 64 / G;
+    const int g = blockIdx.y;
+    const int t = threadIdx.x;
+    const int qi = t / (G * 4), h = (t / 4) % G, sub = t % 4;
+    const int m = blockIdx.x * QB + qi;
+    const bool live = m < M;
+    const int qpos = p0 + (live ? m : M - 1);
+    float q[DS], o[DS];
+    const float *qp = qkv + (long long)(live ? m : M - 1) * P->qkv_rows + (long long)(g * G + h) * hd;
+#pragma unroll
+    for (int e = 0; e < DS; ++e) {
+        q[e] = qp[sub + 4 * e] * P->scale;
+        o[e] = 0.f;
+    }
+    float mx = -INFINITY, l = 0.f;
+    const int last_row = min(M, (blockIdx.x + 1) * QB) - 1;
+    const int kend = p0 + last_row + 1;
+    float *Ks = kvs, *Vs = kvs + PF_KT * hd;
+    const long long rs = (long long)Hkv * hd;
+    for (int kt0 = 0; kt0 < kend; kt0 += PF_KT) {
+        __syncthreads();
+        for (int idx = t; idx < PF_KT * hd; idx += blockDim.x) {
+            const int j = idx / hd, e = idx % hd;
+            const int kp = kt0 + j;
+            float kv = 0.f, vv = 0.f;
+            if (kp < kend) {
+                kv = WTraits<T>::get(kc, (long long)kp * rs + (long long)g * hd + e);
+                vv = WTraits<T>::get(vc, (long long)kp * rs + (long long)g * hd + e);
+            }
+            Ks[idx] = kv;
+            Vs[idx] = vv;
+        }
+        __syncthreads();
+        const int jn = min(PF_KT, kend - kt0);
+        for (int j = 0; j < jn; ++j) {
+            float s = 0.f;
+            const float *kr = Ks + j * hd + sub;
+#pragma unroll
+            for (int e = 0; e < DS; ++e) s = fmaf(q[e], kr[4 * e], s);
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (kt0 + j <= qpos) {
+                if (s > mx) {
+                    const float corr = expf(mx - s);
+                    l *= corr;
+#pragma unroll
+                    for (int e = 0; e < DS; ++e) o[e] *= corr;
+                    mx = s;
+                }
+                const float p = expf(s - mx);
+                l += p;
+                const float *vr = Vs + j * hd + sub;
+#pragma unroll
+                for (int e = 0; e < DS; ++e) o[e] = fmaf(p, vr[4 * e], o[e]);
+            }
+        }
+    }
+    if (live) {
+        float *op = out + (long long)m * P->q_rows + (long long)(g * G + h) * hd;
+#pragma unroll
+        for (int e = 0; e < DS; ++e) op[sub + 4 * e] = o[e] / l;
+    }
+}
+
+__global__ void k_pf_silu(const Plan *__restrict__ P, int M) {
+    const int F = P->F;
+    const long long total = (long long)M * F;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+        const long long m = i / F, k = i - m * F;
+        P->pf_XN[i] = silu_f(P->pf_GU[m * 2 * F + k]) * P->pf_GU[m * 2 * F + F + k];
+    }
+}
+
+__global__ void k_pf_anchor(const Plan *__restrict__ P, int M, int a) {
+    const int d = P->d;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)M * d;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long m = i / d, k = i - m * d;
+        P->pf_ANCH[(m * P->nB + a) * d + k] = P->pf_H[i];
+    }
+}
+
+// logits of one row: pf_logits[v] = W_lm[v] . (rms(h) * g_f)
+template <typename T>
+__global__ void __launch_bounds__(256) k_pf_logits(const Plan *__restrict__ P, const float *__restrict__ h) {
+    extern __shared__ __align__(16) float xs[];
+    __shared__ float red[40];
+    const int d = P->d, V = P->V;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) ss = fmaf(h[k], h[k], ss);
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + P->eps);
+    for (int k = threadIdx.x; k < d; k += blockDim.x) xs[k] = (h[k] * inv) * P->gf[k];
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const T *W = reinterpret_cast<const T *>(P->lm_head);
+    for (int v = blockIdx.x * 8 + warp; v < V; v += gridDim.x * 8) {
+        float acc = 0.f;
+        for (int k = lane; k < d; k += 32) acc = fmaf(WTraits<T>::get(W, (long long)v * d + k), xs[k], acc);
+        acc = warp_sum(acc);
+        if (lane == 0) P->pf_logits[v] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------------
+template <typename T>
+static void pf_layer(const Plan *P, const Plan &h, const LayerW &w, T *kc, T *vc, float *H, int p0, int M,
+                     cudaStream_t s) {
+    const int d = h.d;
+    k_pf_norm<<<M, 256, 0, s>>>(H, h.pf_XN, w.g1, d, h.eps);
+    pf_gemm<T>(h.pf_XN, d, w.wq, h.q_rows, d, h.pf_QKV, h.qkv_rows, M, 0, s);
+    pf_gemm<T>(h.pf_XN, d, w.wk, h.kv_rows, d, h.pf_QKV + h.q_rows, h.qkv_rows, M, 0, s);
+    pf_gemm<T>(h.pf_XN, d, w.wv, h.kv_rows, d, h.pf_QKV + h.q_rows + h.kv_rows, h.qkv_rows, M, 0, s);
+    k_pf_rope_kv<T><<<M, 256, 0, s>>>(P, h.pf_QKV, p0, kc, vc);
+    const int G = h.Hq / h.Hkv, QB = 64 / G;
+    dim3 ag((M + QB - 1) / QB, h.Hkv);
+    const size_t sm = 2 * PF_KT * h.hd * sizeof(float);
+    if (h.hd == 128) k_pf_attn<T, 128><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+    else if (h.hd == 64) k_pf_attn<T, 64><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+    else k_pf_attn<T, 32><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+    pf_gemm<T>(h.pf_ATT, h.q_rows, w.wo, d, h.q_rows, H, d, M, 1, s);
+    k_pf_norm<<<M, 256, 0, s>>>(H, h.pf_XN, w.g2, d, h.eps);
+    pf_gemm<T>(h.pf_XN, d, w.wg, h.F, d, h.pf_GU, 2 * h.F, M, 0, s);
+    pf_gemm<T>(h.pf_XN, d, w.wu, h.F, d, h.pf_GU + h.F, 2 * h.F, M, 0, s);
+    k_pf_silu<<<1024, 256, 0, s>>>(P, M);
+    pf_gemm<T>(h.pf_XN, h.F, w.wd, d, h.F, H, d, M, 1, s);
+}
+
+template <typename T>
+void launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int grid, cudaStream_t s) {
+    (void)grid;
+    for (int p0 = 0; p0 < prompt_len; p0 += h.pf_rows) {
+        const int M = prompt_len - p0 < h.pf_rows ? prompt_len - p0 : h.pf_rows;
+        k_pf_embed<T><<<M, 256, 0, s>>>(P, prompt, p0);
+        for (int l = 0; l < h.L; ++l) {
+            T *kc = reinterpret_cast<T *>(h.kc) + (long long)l * h.kv_stride;
+            T *vc = reinterpret_cast<T *>(h.vc) + (long long)l * h.kv_stride;
+            pf_layer<T>(P, h, h.tl[l], kc, vc, h.pf_H, p0, M, s);
+            if (h.aidx[l + 1] >= 0) k_pf_anchor<<<512, 256, 0, s>>>(P, M, h.aidx[l + 1]);
+        }
+        if (h.Ls > 0) {
+            pf_gemm<T>(h.pf_ANCH, h.nB * h.d, h.proj, h.d, h.nB * h.d, h.pf_Hp, h.d, M, 0, s);
+            for (int l = 0; l < h.Ls; ++l) {
+                T *kc = reinterpret_cast<T *>(h.pkc) + (long long)l * h.kv_stride;
+                T *vc = reinterpret_cast<T *>(h.pvc) + (long long)l * h.kv_stride;
+                pf_layer<T>(P, h, h.pl[l], kc, vc, h.pf_Hp, p0, M, s);
+            }
+        }
+        if (p0 + M == prompt_len)
+            k_pf_logits<T><<<1024, 256, h.d * sizeof(float), s>>>(P, h.pf_H + (long long)(M - 1) * h.d);
+    }
+    launch_prefill_finalize<T>(P, prompt_len, s);
+}
+
+__global__ void k_rope_table(float2 *tab, int max_seq, int half, int hd, double theta) {
+    const long long total = (long long)max_seq * half;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+        const long long p = i / half, j = i - p * half;
+        const double inv = pow(theta, -2.0 * (double)j / (double)hd);
+        const double a = (double)p * inv;
+        tab[i] = make_float2((float)cos(a), (float)sin(a));
+    }
+}
+
+void launch_rope_table(const Plan &h, float theta, cudaStream_t s) {
+    k_rope_table<<<256, 256, 0, s>>>(h.rope, h.max_seq, h.hd / 2, h.hd, (double)theta);
+}
+
+void set_prefill_attributes() {
+    cudaFuncSetAttribute(k_pf_attn<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
+    cudaFuncSetAttribute(k_pf_attn<__nv_bfloat16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
+    cudaFuncSetAttribute(k_pf_logits<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(k_pf_logits<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+}
+
+template void launch_prefill<float>(const Plan *, const Plan &, const int *, int, int, cudaStream_t);
+template void launch_prefill<__nv_bfloat16>(const Plan *, const Plan &, const int *, int, int, cudaStream_t);
+
+}  // namespace spd

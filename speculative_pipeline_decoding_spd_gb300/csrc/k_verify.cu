@@ -1,0 +1,385 @@
+// Streaming verification, commit, rollback and reseed of one pipeline step (one CTA,
+// on the device: no host round trip per step).
+//
+// Speculative pipeline decoding, machine review "What carries the argument":
+// verification is streaming — the token leaving the last stage yields the target's
+// prediction for the next position, which checks the draft one stage behind it; on a
+// rejection the KV cache is truncated after the exiting token, the pipeline is flushed
+// and stage 0 is reseeded with the target's token.  At T > 0 the check is speculative
+// rejection sampling (review "Assumptions", section 3.5, after Leviathan et al.): keep
+// the draft x with probability min(1, p_T(x) / p_D(x)), else draw from the normalised
+// residual max(0, p_T - p_D).
+//
+// Philox stream (the pages only say "seeded Philox uniforms"): counter (t, purpose),
+// purposes 0 draft sample, 1 keep test, 2 target / residual sample, 3 forced coin,
+// 4 forced alternative id; u = (word >> 8) * 2^-24.
+#include "common.cuh"
+
+namespace spd {
+
+constexpr int VT = 256;   // verify kernel threads
+
+__device__ __forceinline__ float u01(uint32_t w) { return (float)(w >> 8) * (1.0f / 16777216.0f); }
+
+// Block-wide inverse-CDF draw over weights w(i), i in [0, V): the smallest i whose running
+// sum (index order) exceeds u * total.  Threads own contiguous index ranges; the range
+// totals are scanned in thread order, the crossing range is scanned sequentially.
+// Returns the index in all threads; *total_out receives the total.
+template <typename WF>
+__device__ int block_sample(int V, float u, WF wf, float *red, float *total_out) {
+    __shared__ float s_part[VT];
+    __shared__ int s_pick;
+    const int per = (V + VT - 1) / VT;
+    const int lo = threadIdx.x * per, hi = min(V, lo + per);
+    float loc = 0.f;
+    for (int i = lo; i < hi; ++i) loc += wf(i);
+    s_part[threadIdx.x] = loc;
+    if (threadIdx.x == 0) s_pick = -1;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int t = 0; t < VT; ++t) tot += s_part[t];
+        red[0] = tot;
+        const float target = u * tot;
+        float acc = 0.f;
+        int th = VT - 1;
+        for (int t = 0; t < VT; ++t) {
+            if (acc + s_part[t] > target && s_part[t] > 0.f) { th = t; break; }
+            acc += s_part[t];
+        }
+        red[1] = acc;
+        red[2] = __int_as_float(th);
+    }
+    __syncthreads();
+    const int th = __float_as_int(red[2]);
+    if ((int)threadIdx.x == th) {
+        float acc = red[1];
+        const float target = u * red[0];
+        int pick = -1, lastnz = -1;
+        for (int i = lo; i < hi; ++i) {
+            const float w = wf(i);
+            if (w > 0.f) lastnz = i;
+            acc += w;
+            if (acc > target && w > 0.f) { pick = i; break; }
+        }
+        s_pick = pick >= 0 ? pick : (lastnz >= 0 ? lastnz : lo);
+    }
+    __syncthreads();
+    if (total_out) *total_out = red[0];
+    const int pick = s_pick;
+    __syncthreads();
+    return pick;
+}
+
+// max and sum of exp(z/T - max) over a logits row (fixed reduction order)
+__device__ void softmax_stats(const float *z, int V, float invT, float *red, float *m_out, float *s_out) {
+    float m = -INFINITY;
+    for (int i = threadIdx.x; i < V; i += blockDim.x) m = fmaxf(m, z[i] * invT);
+    m = block_max(m, red);
+    float s = 0.f;
+    for (int i = threadIdx.x; i < V; i += blockDim.x) s += expf(z[i] * invT - m);
+    s = block_sum(s, red);
+    *m_out = m;
+    *s_out = s;
+}
+
+template <typename T>
+__device__ void embed_into_slot(const Plan *__restrict__ P, int slot, int tok) {
+    const int d = P->d;
+    const T *e = reinterpret_cast<const T *>(P->embed) + (long long)tok * d;
+    float *x = P->X + (long long)slot * d;
+    float *a0 = P->ANCH + (long long)slot * P->nB * d;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) {
+        const float v = WTraits<T>::get(e, k);
+        x[k] = v;
+        a0[k] = v;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
+    __shared__ float red[40];
+    __shared__ int s_done, s_t, s_head, s_ex, s_q, s_x, s_xslot, s_P0, s_newslot, s_draft, s_y, s_ok, s_active;
+    __shared__ float s_tmax, s_tsum;
+    DevState *st = P->st;
+    const int n = P->n, ns = n + 1, V = P->V;
+    const float T_ = P->temperature;
+    if (threadIdx.x == 0) {
+        s_done = st->done;
+        if (!s_done) {
+            const int t = st->t + 1;
+            st->t = t;
+            const int head = st->head;
+            s_t = t;
+            s_head = head;
+            const int s0 = ring(head, 0, ns);
+            s_P0 = st->pos[s0];
+            s_newslot = ring(head + 1, 0, ns);
+            const int exs = ring(head, n - 1, ns);
+            s_ex = st->valid[exs];
+            s_q = st->pos[exs];
+            if (n >= 2) {
+                s_xslot = ring(head, n - 2, ns);
+                s_x = st->tok[s_xslot];
+            } else {
+                s_xslot = s_newslot;
+                s_x = -1;   // the new draft (set below)
+            }
+            // KV valid lengths of the layers that ran, and the bytes streamed
+            int active = 0;
+            for (int s = 0; s < n; ++s) {
+                const int slot = ring(head, s, ns);
+                if (!st->valid[slot]) continue;
+                ++active;
+                for (int l = P->b[s]; l < P->b[s + 1]; ++l) st->len[l] = st->pos[slot] + 1;
+                st->weight_bytes += (double)P->layer_bytes * (P->b[s + 1] - P->b[s]);
+            }
+            st->weight_bytes += (double)(P->pdm_bytes + P->lm_bytes);
+            s_active = active;
+        }
+    }
+    __syncthreads();
+    if (s_done) return;
+    const int t = s_t;
+    // ---- the draft for position P0+1
+    if (threadIdx.x == 0) {
+        int draft;
+        if (P->forced) {
+            const int idx = s_P0 + 1;
+            int r = 0;
+            if (idx < P->forced_ref_len) r = P->forced_ref[idx];
+            else st->error = ERR_FORCED_REF;
+            const uint32_t c = philox_word0((uint32_t)t, 3u, P->seed_lo, P->seed_hi) >> 8;
+            if (c < P->forced_thr) {
+                draft = r;
+            } else {
+                const uint32_t a = philox_word0((uint32_t)t, 4u, P->seed_lo, P->seed_hi) >> 8;
+                const unsigned long long alt = ((unsigned long long)a * (unsigned long long)(V - 1)) >> 24;
+                draft = (int)(((long long)r + 1 + (long long)alt) % V);
+            }
+        } else {
+            draft = st->top[1];
+        }
+        s_draft = draft;
+    }
+    __syncthreads();
+    if (!P->forced && T_ > 0.f) {
+        // sample the draft from softmax(z_D / T) and keep its normalisers with the slot
+        const float *zd = P->dlogits + (long long)s_newslot * V;
+        const float invT = 1.0f / T_;
+        float m, s;
+        softmax_stats(zd, V, invT, red, &m, &s);
+        const float u0 = u01(philox_word0((uint32_t)t, 0u, P->seed_lo, P->seed_hi));
+        const int pick = block_sample(V, u0, [&](int i) { return expf(zd[i] * invT - m); }, red + 4, nullptr);
+        if (threadIdx.x == 0) {
+            s_draft = pick;
+            st->dmax[s_newslot] = m;
+            st->dsum[s_newslot] = s;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0 && n == 1) s_x = s_draft;
+    __syncthreads();
+    // ---- verify the draft behind the exiting token
+    if (s_ex) {
+        if (T_ == 0.f) {
+            if (threadIdx.x == 0) {
+                s_y = st->top[0];
+                s_ok = (s_x == s_y);
+            }
+            __syncthreads();
+        } else {
+            const float invT = 1.0f / T_;
+            const float *zt = P->logits;
+            const float *zd = P->dlogits + (long long)s_xslot * V;
+            float tm, ts;
+            softmax_stats(zt, V, invT, red, &tm, &ts);
+            if (threadIdx.x == 0) {
+                const int x = s_x;
+                const float pt = expf(zt[x] * invT - tm) / ts;
+                const float pd = expf(zd[x] * invT - st->dmax[s_xslot]) / st->dsum[s_xslot];
+                const float u1 = u01(philox_word0((uint32_t)t, 1u, P->seed_lo, P->seed_hi));
+                s_ok = (u1 < pt / pd);
+                s_tmax = tm;
+                s_tsum = ts;
+            }
+            __syncthreads();
+            if (!s_ok) {
+                const float dm = st->dmax[s_xslot], ds = st->dsum[s_xslot];
+                const float tmx = s_tmax, tsm = s_tsum;
+                const float u2 = u01(philox_word0((uint32_t)t, 2u, P->seed_lo, P->seed_hi));
+                float tot;
+                auto resid = [&](int i) {
+                    const float pt = expf(zt[i] * invT - tmx) / tsm;
+                    const float pd = expf(zd[i] * invT - dm) / ds;
+                    return fmaxf(pt - pd, 0.f);
+                };
+                int y = block_sample(V, u2, resid, red + 4, &tot);
+                if (!(tot > 0.f)) y = block_sample(V, u2, [&](int i) { return expf(zt[i] * invT - tmx); }, red + 4, nullptr);
+                if (threadIdx.x == 0) s_y = y;
+            } else if (threadIdx.x == 0) {
+                s_y = s_x;
+            }
+            __syncthreads();
+        }
+    }
+    // ---- commit / rollback / reseed / shift / trace
+    if (threadIdx.x == 0) {
+        const int head = s_head, nh = head + 1;
+        const int ytarget = s_ex ? s_y : -1;
+        int commit = -1, accept = -1;
+        bool flushed = false;
+        if (s_ex) {
+            accept = s_ok;
+            commit = s_ok ? s_x : s_y;
+            st->N += 1;
+            if (st->N < P->max_new) P->out_tokens[st->N] = commit;
+            st->pending = 1;
+            st->pdm_len = s_q + 1;
+            if (s_ok) {
+                st->accepts += 1;
+                st->run_cur += 1;
+            } else {
+                st->rejects += 1;
+                st->run_sum += st->run_cur;
+                st->run_count += 1;
+                st->run_cur = 0;
+                flushed = true;
+                for (int l = 0; l < P->L; ++l) st->len[l] = s_q + 1;
+            }
+        } else {
+            st->pending = 0;
+        }
+        const int ns0 = ring(nh, 0, ns);
+        int newpos, newtok;
+        if (flushed) {
+            newpos = s_q + 1;
+            newtok = s_y;
+            for (int s = 1; s < n; ++s) st->valid[ring(nh, s, ns)] = 0;
+        } else {
+            newpos = s_P0 + 1;
+            newtok = s_draft;
+        }
+        if (newpos >= P->max_seq) {
+            st->error = ERR_SEQ_FULL;
+            st->done = 1;
+            newpos = P->max_seq - 1;
+        }
+        if (newtok < 0 || newtok >= V) {
+            st->error = ERR_TOKEN;
+            newtok = 0;
+        }
+        st->valid[ns0] = 1;
+        st->pos[ns0] = newpos;
+        st->tok[ns0] = newtok;
+        st->head = nh;
+        s_newslot = ns0;
+        s_y = newtok;
+        if (t - 1 < P->max_steps) {
+            spd_trace_rec rec;
+            rec.t = t;
+            rec.exit_pos = s_ex ? s_q : -1;
+            rec.draft = s_ex ? s_x : -1;
+            rec.target = ytarget;
+            rec.accept = accept;
+            rec.commit = commit;
+            rec.pdm_top = st->top[1];
+            rec.new_draft = s_draft;
+            rec.n_committed = st->N;
+            rec.n_active = s_active;
+            rec.target_logit = st->topval[0];
+            rec.pdm_logit = st->topval[1];
+            P->trace[t - 1] = rec;
+            for (int l = 0; l < P->L; ++l) P->trace_len[(long long)(t - 1) * P->L + l] = st->len[l];
+        } else {
+            st->error = ERR_TRACE_FULL;
+            st->done = 1;
+        }
+        if (1 + st->N >= P->max_new) st->done = 1;
+    }
+    __syncthreads();
+    embed_into_slot<T>(P, s_newslot, s_y);
+}
+
+// First token after the prefill (greedy argmax, or a draw with uniform (0, purpose 2)),
+// then the initial pipeline state: y0 committed and seeded into stage 0 (slot 0).
+template <typename T>
+__global__ void __launch_bounds__(VT) k_prefill_finalize(const Plan *__restrict__ P, int prompt_len) {
+    __shared__ float red[40];
+    __shared__ float s_bv[VT / 32];
+    __shared__ int s_bi[VT / 32];
+    __shared__ int s_y;
+    DevState *st = P->st;
+    const int V = P->V;
+    const float *z = P->pf_logits;
+    if (P->temperature > 0.f) {
+        const float invT = 1.0f / P->temperature;
+        float m, s;
+        softmax_stats(z, V, invT, red, &m, &s);
+        const float u = u01(philox_word0(0u, 2u, P->seed_lo, P->seed_hi));
+        const int y = block_sample(V, u, [&](int i) { return expf(z[i] * invT - m); }, red + 4, nullptr);
+        if (threadIdx.x == 0) s_y = y;
+    } else {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int i = threadIdx.x; i < V; i += blockDim.x) {
+            const float v = z[i];
+            if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if ((threadIdx.x & 31) == 0) { s_bv[threadIdx.x >> 5] = bv; s_bi[threadIdx.x >> 5] = bi; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float b = -INFINITY;
+            int id = 0x7fffffff;
+            for (int w = 0; w < VT / 32; ++w)
+                if (s_bv[w] > b || (s_bv[w] == b && s_bi[w] < id)) { b = s_bv[w]; id = s_bi[w]; }
+            s_y = id;
+            st->topval[0] = b;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int y0 = s_y;
+        st->head = 0;
+        st->t = 0;
+        st->N = 0;
+        st->done = P->max_new <= 1 ? 1 : 0;
+        st->pending = 0;
+        st->error = 0;
+        st->pdm_len = prompt_len;
+        st->prompt_len = prompt_len;
+        for (int i = 0; i < MAXS; ++i) st->valid[i] = 0;
+        st->valid[0] = 1;
+        st->pos[0] = prompt_len;
+        st->tok[0] = y0;
+        for (int l = 0; l < P->L; ++l) st->len[l] = prompt_len;
+        st->top[0] = y0;
+        st->top[1] = -1;
+        st->accepts = st->rejects = st->run_cur = st->run_sum = st->run_count = 0;
+        st->weight_bytes = 0.0;
+        P->out_tokens[0] = y0;
+    }
+    __syncthreads();
+    embed_into_slot<T>(P, 0, s_y);
+}
+
+template <typename T>
+void launch_verify(const Plan *P, const Plan &h, cudaStream_t s) {
+    k_verify<T><<<1, VT, 0, s>>>(P);
+}
+template <typename T>
+void launch_prefill_finalize(const Plan *P, int prompt_len, cudaStream_t s) {
+    k_prefill_finalize<T><<<1, VT, 0, s>>>(P, prompt_len);
+}
+template void launch_verify<float>(const Plan *, const Plan &, cudaStream_t);
+template void launch_verify<__nv_bfloat16>(const Plan *, const Plan &, cudaStream_t);
+template void launch_prefill_finalize<float>(const Plan *, int, cudaStream_t);
+template void launch_prefill_finalize<__nv_bfloat16>(const Plan *, int, cudaStream_t);
+
+}  // namespace spd

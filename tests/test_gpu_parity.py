@@ -1,0 +1,122 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Integer results (token ids, keep decisions, commits, exit positions, per-layer KV valid
+lengths) must agree exactly; where the oracle's own decision is within the tolerance of
+a tie (top-2 logit margin <= tol * |top-1|) it follows the GPU's choice (replay rule).
+Logits agree within rel 1e-4 (fp32 weights) or 2e-2 (bf16 weights), relative to
+max(1, |logit|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import spd_inputs as si
+from gpu_common import Case, ar_reference, compare, engine, materialise, replay_oracle, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+TINY = Case(si.TINY.dims, n=2, anchors=(0, 2, 4), Ls=1, prompt_len=16, max_new=64)
+# bf16, hd 64, GQA 2, prompt long enough for several 128-position attention chunks + tail
+SMALL = Case(si.ModelDims(L=6, d=256, Hq=4, Hkv=2, hd=64, F=512, V=2000), n=3, anchors=(0, 3, 6), Ls=2,
+             prompt_len=300, max_new=48, norms="perturbed")
+# bf16, hd 128, GQA 4 (the 4B shape's head layout), 5 layers over 4 stages (ragged stages)
+HD128 = Case(si.ModelDims(L=5, d=512, Hq=8, Hkv=2, hd=128, F=1024, V=3000), n=4, anchors=(0, 2, 5), Ls=1,
+             prompt_len=140, max_new=40, norms="perturbed")
+
+
+def _prefill_logits_close(case, pf):
+    tg, pd, prompt, m, _, _ = materialise(case)
+    from oracle import SPDOracle
+    o = SPDOracle(m, case.n, case.max_seq)
+    o.prefill(prompt)
+    z = o.prefill_logits
+    err = np.max(np.abs(pf - z)) / max(1.0, np.max(np.abs(z)))
+    assert err <= case.tol, err
+    return err
+
+
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128], ids=["tiny", "small", "hd128"])
+def test_prefill_logits(case):
+    toks, tr, st, pf = run_gpu(case, force_p=1.0, forced_ref=torch.zeros(case.max_seq, dtype=torch.int32).cuda())
+    _prefill_logits_close(case, pf)
+
+
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128], ids=["tiny", "small", "hd128"])
+def test_greedy_draft_module_replay(case):
+    toks, tr, st, pf = run_gpu(case)
+    o, rep = replay_oracle(case, tr, toks)
+    compare(case, tr, o, rep)
+    assert o.tokens[case.prompt_len:] == toks
+    assert st["N"] == case.max_new - 1 and st["K"] == len(tr)
+
+
+@pytest.mark.parametrize("case,p", [(TINY, 0.6), (SMALL, 0.5), (SMALL, 0.9), (HD128, 0.7)],
+                         ids=["tiny-0.6", "small-0.5", "small-0.9", "hd128-0.7"])
+def test_forced_draft_replay(case, p):
+    ar = ar_reference(case)
+    tg, pd, prompt, m, _, _ = materialise(case)
+    ref = np.array(list(prompt) + ar + [0] * (case.n + 8), dtype=np.int32)
+    toks, tr, st, pf = run_gpu(case, force_p=p, forced_ref=torch.from_numpy(ref).cuda(), seed=5)
+    o, rep = replay_oracle(case, tr, toks, forced_p=p, forced_ref=ref, seed=5)
+    compare(case, tr, o, rep)
+    assert o.tokens[case.prompt_len:] == toks
+    assert st["accepts"] > 0 and st["rejects"] > 0
+
+
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128], ids=["tiny", "small", "hd128"])
+def test_pipeline_equals_single_stage_bitwise(case):
+    """Losslessness on the device: for every n the pipelined decode commits the same
+    tokens as n = 1 (one token through all layers per step), and the per-step target
+    logits are bit-identical, because no kernel's arithmetic depends on which stages
+    share a launch."""
+    ar_toks, ar_tr, _, _ = run_gpu(case, n=1)
+    ar_logit = {r["exit_pos"]: r["target_logit"] for r in ar_tr if r["exit_pos"] >= 0}
+    for n in sorted({2, case.n, min(case.dm.L, 5)}):
+        toks, tr, st, _ = run_gpu(case, n=n)
+        assert toks == ar_toks, n
+        for r in tr:
+            if r["exit_pos"] >= 0:
+                assert r["target_logit"] == ar_logit[r["exit_pos"]], (n, r["exit_pos"])
+
+
+def test_graph_and_eager_agree():
+    a = run_gpu(SMALL, graph=False)[:2]
+    b = run_gpu(SMALL, graph=True)[:2]
+    assert a[0] == b[0] and [r["len"] for r in a[1]] == [r["len"] for r in b[1]]
+
+
+def test_host_buffers_generate():
+    tg, pd, prompt, m, _, _ = materialise(SMALL)
+    e = engine(SMALL)
+    host_toks, st = e.generate(prompt, on_host=True)
+    e.close()
+    dev_toks = run_gpu(SMALL)[0]
+    assert host_toks == dev_toks
+
+
+def test_step_by_step_state_matches_oracle_hidden_states():
+    """Residual stream of every in-flight slot after each of the first steps, against
+    the oracle's in-flight hidden states (same tolerance)."""
+    case = SMALL
+    tg, pd, prompt, m, _, _ = materialise(case)
+    e = engine(case, graph=False)
+    e.prefill(torch.from_numpy(prompt).cuda())
+    from oracle import Replay, SPDOracle
+    gtr = []
+    o = None
+    for k in range(1, 9):
+        e.step(1)
+        tr = e.trace()
+        o, rep = replay_oracle(case, tr, e.tokens(), max_steps=k)
+        X = e.read(0, (case.n + 1, case.dm.d))
+        slots = e.read(7, (3, case.n + 1), dtype=np.int32)
+        for s, tk in enumerate(o.slots):
+            if tk is None or s == 0:
+                continue      # stage 0 holds a just-embedded token
+            # find the slot holding this position
+            idx = [i for i in range(case.n + 1) if slots[0][i] and slots[1][i] == tk.pos]
+            assert idx, (k, tk.pos)
+            ref = tk.H[0]
+            err = np.max(np.abs(X[idx[0]] - ref)) / max(1.0, np.max(np.abs(ref)))
+            assert err <= case.tol, (k, s, err)
+    e.close()
