@@ -1,0 +1,368 @@
+"""Throughput of the speculative-pipeline-decoding step on the 4B shape (n = 8).
+
+One bench "step" is one pipeline step: every occupied stage runs its layers on its own
+token, the draft module runs on the second stream, then the LM head and device-side
+verification / rollback.  The timed region is K consecutive steps of a 512-token
+generation after the (untimed) prefill; value = committed tokens / device time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--mode forced-0.6]
+
+Multi-GPU: independent replicas (one sequence per GPU, no collective on the data path);
+value = all ranks' committed tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import spd_inputs as si  # noqa: E402
+
+METRIC = "committed tokens/s + step us (4B-shape bf16, n=8); weight GB/s vs 8 TB/s HBM"
+WL = si.SHAPE_4B
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--mode", default="forced-0.6", help="forced-<p> or greedy (draft-module argmax)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: leave out the host-buffer leg")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling runs only: a smaller case of the same kernels (L layers, anchors scaled)")
+    return ap.parse_args()
+
+
+def mode_p(mode: str):
+    return float(mode.split("-", 1)[1]) if mode.startswith("forced-") else None
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce(x: float, op, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=op)
+    return float(t.item())
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f:
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1]))
+                mx = float(c[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, c[5:9]):
+                if v.lower() in ("active", "0x1") or v == "1":
+                    reasons.add(nm)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def stage_sizes(L, n):
+    b = [(s * L) // n for s in range(n + 1)]
+    return [b[s + 1] - b[s] for s in range(n)]
+
+
+def gateup_bytes(trace, dm, n):
+    """Algorithmic bytes of every gate/up launch in the traced steps: per launch (round j)
+    the occupied stages that hold a j-th layer stream 2 x F x d bf16 weights."""
+    sizes = stage_sizes(dm.L, n)
+    J = max(sizes)
+    per = 2 * dm.F * dm.d * 2
+    tot, launches = 0, 0
+    for r in trace:
+        m = r["n_active"]
+        for j in range(J):
+            tot += per * sum(1 for s in range(m) if j < sizes[s])
+            launches += 1
+    return tot, launches
+
+
+# ---------------------------------------------------------------------------------------
+def run_gb300(args, ws, rank, local):
+    from speculative_pipeline_decoding_spd_gb300.engine import Engine
+    dm, n = WL.dims, WL.n
+    p = mode_p(args.mode)
+    with si.on_device("cuda"):
+        tg = si.make_target(dm, 0)
+        pd = si.make_pdm(dm, WL.Ls, len(WL.anchors), 0)
+    prompt = torch.from_numpy(si.make_prompt(dm.V, WL.prompt_len, 1 + rank)).cuda()
+    # the generation must outlast warmup + timed steps
+    alpha_lo = 1.0 / n if p is None else 1.0 / (1.0 + (n - 1) * (1.0 - p))
+    max_new = max(WL.max_new, int(math.ceil((args.warmup + args.steps + 2 * n) * min(1.0, alpha_lo * 1.3))) + 8)
+    max_seq = WL.prompt_len + max_new + n + 8
+    forced_ref = None
+    if p is not None:
+        # forced drafts follow this implementation's own greedy stream (one stage = plain decode)
+        ar = Engine(dm, tg, pd, 1, WL.anchors, max_seq=max_seq, max_new=max_new + n + 2, graph=True)
+        out, cnt, _ = ar.generate(prompt)
+        forced_ref = torch.cat([prompt, out[:cnt], torch.zeros(n + 8, dtype=torch.int32, device="cuda")]).contiguous()
+        ar.close()
+    e = Engine(dm, tg, pd, n, WL.anchors, max_seq=max_seq, max_new=max_new, seed=2,
+               force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True, timing=True)
+    e.prefill(prompt)
+    e.step(args.warmup)
+    t0_ms, l0 = e.kernel_timing()
+    N0 = e.stats()["N"]
+    K0 = e.stats()["K"]
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = Clocks(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.cudart().cudaProfilerStart()   # ncu --profile-from-start off captures only the timed region
+    ev0.record()
+    left = args.steps
+    while left > 0:
+        k = min(8, left)
+        e.step(k)
+        left -= k
+    ev1.record()
+    torch.cuda.synchronize()
+    torch.cuda.cudart().cudaProfilerStop()
+    clocks = clk.stop()
+    barrier(ws)
+    ms = ev0.elapsed_time(ev1)
+    st = e.stats()
+    N1, K1 = st["N"], st["K"]
+    assert K1 - K0 == args.steps, "generation ended inside the timed region"
+    t1_ms, l1 = e.kernel_timing()
+    tr = e.trace()[K0:K1]
+    commits = N1 - N0
+    # weight bytes streamed by the timed steps (occupied stages + draft module + LM head)
+    sizes = stage_sizes(dm.L, n)
+    el = 2
+    layer_b = el * ((dm.Hq + 2 * dm.Hkv) * dm.hd * dm.d + dm.d * dm.Hq * dm.hd + 3 * dm.F * dm.d)
+    pdm_b = el * (dm.d * len(WL.anchors) * dm.d) + WL.Ls * layer_b
+    lm_b = el * dm.V * dm.d
+    wbytes = sum(layer_b * sum(sizes[s] for s in range(r["n_active"])) for r in tr) + len(tr) * (pdm_b + lm_b)
+    gb, gl = gateup_bytes(tr, dm, n)
+    g_ms = t1_ms - t0_ms
+    assert l1 - l0 == gl, (l1 - l0, gl)
+    e.close()
+    del e
+
+    # ---- end to end through the public call with host buffers (prefill included)
+    if args.skip_e2e:
+        return dict(ms=ms, commits=commits, steps=args.steps, wbytes=wbytes, gate_bytes=gb, gate_ms=g_ms,
+                    gate_launches=gl, clocks=clocks, alpha=commits / args.steps, e2e_tokens=0, e2e_s=float("nan"),
+                    e2e_steps=1, max_new=max_new, prompt_len=WL.prompt_len,
+                    launches_per_step=5 * max(sizes) + 1 + 5 * WL.Ls + 2)
+    e2 = Engine(dm, tg, pd, n, WL.anchors, max_seq=WL.prompt_len + WL.max_new + n + 8, max_new=WL.max_new, seed=2,
+                force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True)
+    host_prompt = prompt.cpu().numpy()
+    e2.generate(host_prompt, on_host=True)   # warm
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    toks, st2 = e2.generate(host_prompt, on_host=True)
+    e2_s = time.perf_counter() - t
+    e2_steps = st2.K
+    e2.close()
+    return dict(ms=ms, commits=commits, steps=args.steps, wbytes=wbytes, gate_bytes=gb, gate_ms=g_ms, gate_launches=gl,
+                clocks=clocks, alpha=commits / args.steps, e2e_tokens=len(toks), e2e_s=e2_s, e2e_steps=e2_steps,
+                max_new=max_new, prompt_len=WL.prompt_len, launches_per_step=5 * max(sizes) + 1 + 5 * WL.Ls + 2)
+
+
+# ---------------------------------------------------------------------------------------
+def oracle_sample(n_steps: int, prompt_len: int = 32):
+    """The CPU oracle on the same shape: fp64 model, short prompt (prefill untimed), then
+    n_steps pipeline steps timed on all host cores.  Returns (steps/s, seconds, cores)."""
+    from oracle import Model, SPDOracle
+    dm = WL.dims
+    tg = si.make_target(dm, 0)
+    pd = si.make_pdm(dm, WL.Ls, len(WL.anchors), 0)
+    m = Model(dm, tg, pd, WL.anchors)
+    del tg, pd
+    prompt = si.make_prompt(dm.V, prompt_len, 1)
+    o = SPDOracle(m, WL.n, prompt_len + n_steps + WL.n + 8)
+    o.prefill(prompt)
+    t = time.perf_counter()
+    for _ in range(n_steps):
+        o.step()
+    dt = time.perf_counter() - t
+    return n_steps / dt, dt, os.cpu_count()
+
+
+def main():
+    args = parse()
+    global WL
+    if args.layers:
+        L = args.layers
+        WL = si.Workload(f"{WL.name}-L{L}", si.shrink(WL.dims, L=L), n=min(WL.n, L),
+                         anchors=tuple(sorted({round(a * L / 36) for a in WL.anchors})), Ls=min(WL.Ls, max(1, L // WL.n)),
+                         prompt_len=WL.prompt_len, max_new=WL.max_new)
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        return main_reference(args, ws, rank)
+    torch.cuda.set_device(local)
+    pk, pk_kind = peaks()
+    r = run_gb300(args, ws, rank, local)
+    ms_max = allreduce(r["ms"], _max_op(), ws)
+    commits_all = allreduce(float(r["commits"]), _sum_op(), ws)
+    if rank != 0:
+        return
+    p = mode_p(args.mode)
+    value = commits_all / (ms_max / 1e3)
+    hbm = pk["hbm_gbs"]
+    g_ach = r["gate_bytes"] / (r["gate_ms"] / 1e3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "gateup_traffic.json")
+    if os.path.exists(tp):
+        tj = json.load(open(tp))
+        src = os.path.join(ROOT, "speculative_pipeline_decoding_spd_gb300", "csrc", "k_target.cu")
+        if tj.get("k_target_sha") == source_hash(src):
+            per_stage_layer = tj["dram_bytes_per_stage_layer"]
+            traffic = per_stage_layer * (r["gate_bytes"] / (2 * WL.dims.F * WL.dims.d * 2)) / r["gate_launches"]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "committed tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights drawn on the GPU, uniform-random prompt ids)",
+        "config": {"workload": f"{WL.name}: L36 d2560 32q/8kv x128 F9728 V151936, n=8, Ls=4, anchors 0,9,18,27,35, "
+                               f"prompt {WL.prompt_len}, {args.mode}",
+                   "mode": args.mode, "n": WL.n, "prompt_len": WL.prompt_len, "max_new": r["max_new"],
+                   "parallelism": f"replicas x{ws}", "l2": "no flush needed: ~9 GB of weights per step >> 129 MB L2",
+                   "alpha": round(r["alpha"], 4), "S0": round(r["alpha"] * WL.n, 3),
+                   "weight_GBps": round(r["wbytes"] / (r["ms"] / 1e3) / 1e9, 1),
+                   "weight_frac_of_hbm": round(r["wbytes"] / (r["ms"] / 1e3) / 1e9 / hbm, 4)},
+        "roofline": {"kernel": "target gate/up GEMV (k_target_gemv EPI_GATEUP)", "bound": "hbm",
+                     "achieved": round(g_ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(g_ach / hbm, 4),
+                     "traffic": None if traffic is None else round(traffic), "peak_kind": f"hbm_gbs ({pk_kind})",
+                     "launches": r["gate_launches"]},
+        "clocks": r["clocks"],
+        "e2e": {"value": round(r["e2e_tokens"] / r["e2e_s"], 2), "unit": "generated tokens/s (spd_generate, host "
+                "buffers, prefill + decode)", "h2d_bytes_per_step": round(4 * r["prompt_len"] / r["e2e_steps"], 3),
+                "d2h_bytes_per_step": round((4 * WL.max_new + 32 * math.ceil(r["e2e_steps"] / 8)) / r["e2e_steps"], 3)},
+        "gpu_launches": r["launches_per_step"] * args.steps,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        try:
+            sps, dt, cores = oracle_sample(12)
+            alpha = r["alpha"]
+            line["cpu_baseline"] = {"value": round(sps * alpha, 4), "unit": "committed tokens/s", "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": f"fp64 oracle, same 4B shape n=8, 32-token prompt (prefill untimed), 12 "
+                                              f"pipeline steps timed ({dt:.1f} s); tokens/s = steps/s x alpha {alpha:.3f} "
+                                              f"of the GPU run"}
+        except MemoryError as ex:
+            line["cpu_baseline"] = {"value": None, "unit": "committed tokens/s", "cores": os.cpu_count(),
+                                    "kind": "oracle", "sample": f"not run: {ex}"}
+    print(json.dumps(line), flush=True)
+
+
+def _max_op():
+    import torch.distributed as dist
+    return dist.ReduceOp.MAX
+
+
+def _sum_op():
+    import torch.distributed as dist
+    return dist.ReduceOp.SUM
+
+
+def main_reference(args, ws, rank):
+    """The oracle (plain fp64 CPU restatement of the method) on this arm's workload."""
+    if rank != 0:
+        return
+    k = max(1, min(args.steps, 12))
+    w = max(0, min(args.warmup, 2))
+    from oracle import closed_form_alpha
+    p = mode_p(args.mode)
+    alpha = closed_form_alpha(WL.n, p) if p is not None else 1.0 / WL.n
+    sps, dt, cores = oracle_sample(k + w)
+    value = sps * alpha
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "committed tokens/s", "n_gpus": 1,
+        "steps": k, "warmup": w, "ms_per_step": round(1e3 / sps, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WL.name}, n=8, {args.mode}", "mode": args.mode},
+        "cpu_baseline": {"value": round(value, 4), "unit": "committed tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"fp64 oracle, 4B shape n=8, 32-token prompt (prefill untimed), {k + w} steps "
+                                   f"({dt:.1f} s); tokens/s = steps/s x closed-form alpha {alpha:.3f}"},
+        "e2e": {"value": round(value, 4), "unit": "committed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

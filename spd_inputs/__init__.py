@@ -73,9 +73,12 @@ def _tensor_seed(base: int, name: str) -> int:
     return int(h[:15], 16)
 
 
+_DEVICE = "cpu"
+
+
 def _normal(shape, base: int, name: str, std: float) -> torch.Tensor:
-    g = torch.Generator().manual_seed(_tensor_seed(base, name))
-    return torch.randn(*shape, generator=g, dtype=torch.float32) * std
+    g = torch.Generator(device=_DEVICE).manual_seed(_tensor_seed(base, name))
+    return torch.randn(*shape, generator=g, dtype=torch.float32, device=_DEVICE) * std
 
 
 def _store(t: torch.Tensor, dtype: str) -> torch.Tensor:
@@ -84,7 +87,7 @@ def _store(t: torch.Tensor, dtype: str) -> torch.Tensor:
 
 def _norm_gain(d: int, base: int, name: str, norms: str) -> torch.Tensor:
     if norms == "ones":
-        return torch.ones(d, dtype=torch.float32)
+        return torch.ones(d, dtype=torch.float32, device=_DEVICE)
     return 1.0 + _normal((d,), base, name, 0.1)
 
 
@@ -133,6 +136,23 @@ def make_pdm(dm: ModelDims, Ls: int, n_anchors: int, seed: int = 0, norms: str =
     }
 
 
+class on_device:
+    """Draw the tensors directly on a device with that device's generator (same seeds and
+    distribution, different values from the CPU draw).  For throughput runs whose
+    weights the oracle never needs."""
+
+    def __init__(self, device: str):
+        self.device = device
+
+    def __enter__(self):
+        global _DEVICE
+        self.prev, _DEVICE = _DEVICE, self.device
+
+    def __exit__(self, *a):
+        global _DEVICE
+        _DEVICE = self.prev
+
+
 def make_prompt(V: int, length: int, seed: int = 1) -> np.ndarray:
     g = torch.Generator().manual_seed(seed)
     return torch.randint(0, V, (length,), generator=g, dtype=torch.int64).numpy().astype(np.int32)
@@ -156,4 +176,4 @@ def workload(name: str) -> Workload:
 
 __all__ = ["ModelDims", "Workload", "WORKLOADS", "TINY", "SHAPE_06B", "SHAPE_4B", "SHAPE_8B",
            "SHAPE_4B_T1", "make_target", "make_pdm", "make_layer", "make_prompt", "to_f64",
-           "layer_shapes", "LAYER_MATS", "shrink", "workload"]
+           "layer_shapes", "LAYER_MATS", "shrink", "workload", "on_device"]
