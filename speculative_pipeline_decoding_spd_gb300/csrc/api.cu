@@ -92,6 +92,7 @@ static int validate(const spd_dims *d, int Ls, const spd_config *c, std::string 
     if (Ls < 0 || Ls > SPD_MAX_PDM_LAYERS) { why = "Ls out of range"; return SPD_EINVAL; }
     if (c->max_new < 1) { why = "max_new < 1"; return SPD_EINVAL; }
     if (c->max_seq < c->max_new + c->n + 1) { why = "max_seq too small"; return SPD_EINVAL; }
+    if (c->max_seq > 16384) { why = "max_seq above 16384 (attention merges at most 128 chunks)"; return SPD_EINVAL; }
     if (!(c->temperature >= 0.f)) { why = "temperature < 0"; return SPD_EINVAL; }
     if (c->force_p >= 0.f) {
         if (c->force_p > 1.f) { why = "force_p > 1"; return SPD_EINVAL; }
@@ -337,6 +338,7 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
     set_target_attributes(std::max(gsm, 48 * 1024));
     set_pdm_attributes(std::max(H->sk.smem, 48 * 1024));
     set_prefill_attributes();
+    set_attn_attributes();
     H->grid_gemv = H->num_sms * target_blocks_per_sm(h.dtype, gemv_smem_bytes(h));
     H->grid_lm = std::min(LM_GRID_MAX, H->num_sms * lm_blocks_per_sm(h.dtype, 2 * h.d * 4, h.pdm_lm_head == h.lm_head));
     if (cudaStreamCreateWithFlags(&H->s_main, cudaStreamNonBlocking) != cudaSuccess ||

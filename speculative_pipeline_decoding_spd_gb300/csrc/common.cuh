@@ -198,6 +198,67 @@ __device__ __forceinline__ float block_max(float v, float *red) {
     return red[32];
 }
 
+// Copy n floats (n % 4 == 0, both 16-byte aligned) from global to shared memory with up
+// to 8 16-byte loads per thread in flight before any store.  Kept out of line so that its
+// staging registers do not count against the caller's main loop.
+static __device__ __noinline__ void stage_f4(const float *__restrict__ src, float *dst, int n) {
+    const int n4 = n >> 2;
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    for (int b = threadIdx.x; b < n4; b += 8 * blockDim.x) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * blockDim.x;
+            if (i < n4) v[u] = s4[i];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * blockDim.x;
+            if (i < n4) d4[i] = v[u];
+        }
+    }
+}
+
+// x staging of a normalised input: xs = rms(x) * g.  x is staged first, the statistics
+// come from shared memory with a fixed-order block reduction.  Ends with __syncthreads.
+static __device__ __noinline__ void stage_norm(const float *__restrict__ x, const float *__restrict__ g, int d, float eps,
+                                        float *xs, float *red) {
+    stage_f4(x, xs, d);
+    __syncthreads();
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) {
+        const float v = xs[k];
+        ss = fmaf(v, v, ss);
+    }
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    const int d4 = d >> 2;
+    const float4 *g4 = reinterpret_cast<const float4 *>(g);
+    float4 *x4 = reinterpret_cast<float4 *>(xs);
+    for (int b = threadIdx.x; b < d4; b += 8 * blockDim.x) {
+        float4 gv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * blockDim.x;
+            if (i < d4) gv[u] = g4[i];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * blockDim.x;
+            if (i < d4) {
+                float4 v = x4[i];
+                v.x = (v.x * inv) * gv[u].x;
+                v.y = (v.y * inv) * gv[u].y;
+                v.z = (v.z * inv) * gv[u].z;
+                v.w = (v.w * inv) * gv[u].w;
+                x4[i] = v;
+            }
+        }
+    }
+    __syncthreads();
+}
+
 __device__ __forceinline__ int ring(int head, int s, int nslots) {
     int r = (head - s) % nslots;
     return r < 0 ? r + nslots : r;
@@ -274,6 +335,8 @@ void sk_plan(const Plan &h, int num_sms, SkPlan &sk);
 void set_pdm_attributes(int smem);
 void set_target_attributes(int smem);
 void set_prefill_attributes();
+void set_attn_attributes();
+int attn_smem_bytes(int dtype, int hd);
 template <typename T> void launch_verify(const Plan *P, const Plan &h, cudaStream_t s);
 template <typename T> void launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int grid,
                                           cudaStream_t s);

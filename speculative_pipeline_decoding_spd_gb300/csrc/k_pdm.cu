@@ -82,7 +82,6 @@ __global__ void __launch_bounds__(SK_THREADS) k_skinny(const Plan *__restrict__ 
     extern __shared__ __align__(16) unsigned char sk_smem[];
     __shared__ PdmRows pr;
     __shared__ int s_done, s_last, s_glast;
-    __shared__ float red[33];
     if (threadIdx.x == 0) {
         s_done = P->st->done;
         build_pdm_rows(P, pr);
@@ -99,14 +98,26 @@ __global__ void __launch_bounds__(SK_THREADS) k_skinny(const Plan *__restrict__ 
     const int pitch = kmax + (sizeof(XT) == 2 ? 32 : 4);   // elements; keeps 16-byte rows off one bank
     XT *xs = reinterpret_cast<XT *>(sk_smem);
 
-    // ---- stage the R activation rows of this K segment
-    for (int idx = threadIdx.x; idx < RP * kseg; idx += blockDim.x) {
-        const int r = idx / kseg, kk = idx - r * kseg;
-        const float v = r < R ? sk_xval<XM>(P, pr, layer, r, k0 + kk) : 0.f;
-        if (sizeof(XT) == 2)
-            reinterpret_cast<__nv_bfloat16 *>(xs)[r * pitch + kk] = __float2bfloat16_rn(v);
-        else
-            reinterpret_cast<float *>(xs)[r * pitch + kk] = v;
+    // ---- stage the R activation rows of this K segment (8 loads in flight per thread)
+    const int total = RP * kseg;
+    for (int b = threadIdx.x; b < total; b += 8 * blockDim.x) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = b + u * blockDim.x;
+            const int r = idx / kseg, kk = idx - r * kseg;
+            v[u] = (idx < total && r < R) ? sk_xval<XM>(P, pr, layer, r, k0 + kk) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int idx = b + u * blockDim.x;
+            if (idx >= total) continue;
+            const int r = idx / kseg, kk = idx - r * kseg;
+            if (sizeof(XT) == 2)
+                reinterpret_cast<__nv_bfloat16 *>(xs)[r * pitch + kk] = __float2bfloat16_rn(v[u]);
+            else
+                reinterpret_cast<float *>(xs)[r * pitch + kk] = v[u];
+        }
     }
     __syncthreads();
 
@@ -207,20 +218,48 @@ __global__ void __launch_bounds__(SK_THREADS) k_skinny(const Plan *__restrict__ 
     if (!s_last) return;
     __threadfence();
 
-    // ---- epilogue for rows [rb*128, rb*128+128): sum the K-split partials in order
+    // ---- epilogue for rows [rb*128, rb*128+128): sum the K-split partials in split order.
+    // Each thread owns items tid, tid+256, ...; the loads of 4 items x 8 splits are issued
+    // before any add, so the chain costs a few L2 round trips, not nks of them.
     const int rlo = rb * SK_ROWS, rhi = min(N, rlo + SK_ROWS);
     const int d = P->d;
     float *ys = reinterpret_cast<float *>(sk_smem);   // [128][RP] (reuses the x buffer)
     __syncthreads();
-    for (int idx = threadIdx.x; idx < (rhi - rlo) * R; idx += blockDim.x) {
-        const int rl = idx / R, r = idx - rl * R;
-        const int row = rlo + rl;
-        float sum = 0.f;
-        for (int q = 0; q < nks; ++q) sum += __ldcg(part + ((long long)q * N + row) * RP + r);
-        if (SE == SE_PROJ) P->Xp[(long long)r * d + row] = sum;
-        else if (SE == SE_OPROJ || SE == SE_DOWN) P->Xp[(long long)r * d + row] += sum;
-        else if (SE == SE_GATEUP) P->GUp[(long long)r * 2 * P->F + row] = sum;
-        else ys[rl * RP + r] = sum;
+    const int nitems = (rhi - rlo) * R;
+    for (int i0 = threadIdx.x; i0 < nitems; i0 += 4 * blockDim.x) {
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        long long base[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = min(i0 + e * (int)blockDim.x, nitems - 1);
+            const int rl = idx / R, r = idx - rl * R;
+            base[e] = (long long)(rlo + rl) * RP + r;
+        }
+        for (int q0 = 0; q0 < nks; q0 += 8) {
+            float v[4][8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    v[e][u] = (i0 + e * (int)blockDim.x < nitems && q0 + u < nks)
+                                  ? __ldcg(part + (long long)(q0 + u) * N * RP + base[e]) : 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (q0 + u < nks) sum[e] += v[e][u];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = i0 + e * blockDim.x;
+            if (idx >= nitems) continue;
+            const int rl = idx / R, r = idx - rl * R;
+            const int row = rlo + rl;
+            if (SE == SE_PROJ) P->Xp[(long long)r * d + row] = sum[e];
+            else if (SE == SE_OPROJ || SE == SE_DOWN) P->Xp[(long long)r * d + row] += sum[e];
+            else if (SE == SE_GATEUP) P->GUp[(long long)r * 2 * P->F + row] = sum[e];
+            else ys[rl * RP + r] = sum[e];
+        }
     }
     if (SE == SE_QKV) {
         __syncthreads();
@@ -260,14 +299,31 @@ __global__ void __launch_bounds__(SK_THREADS) k_skinny(const Plan *__restrict__ 
         __syncthreads();
         if (!s_glast) return;
         __threadfence();
-        for (int r = 0; r < R; ++r) {
-            float ss = 0.f;
-            for (int k = threadIdx.x; k < d; k += blockDim.x) {
-                const float v = __ldcg(P->Xp + (long long)r * d + k);
-                ss = fmaf(v, v, ss);
-            }
-            ss = block_sum(ss, red);
-            if (threadIdx.x == 0) P->inv_rms_p[r] = 1.0f / sqrtf(ss / (float)d + P->eps);
+        // all rows at once: per-thread sums of squares with the rows' loads in flight
+        // together, then one fixed-order reduction over warps per row
+        float ss[RP];
+#pragma unroll
+        for (int r = 0; r < RP; ++r) ss[r] = 0.f;
+        for (int k = threadIdx.x; k < d; k += blockDim.x) {
+#pragma unroll
+            for (int r = 0; r < RP; ++r)
+                if (r < R) {
+                    const float v = __ldcg(P->Xp + (long long)r * d + k);
+                    ss[r] = fmaf(v, v, ss[r]);
+                }
+        }
+        float *wred = reinterpret_cast<float *>(sk_smem);   // [8 warps][RP]
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+            const float t = warp_sum(ss[r]);
+            if (lane == 0) wred[warp * RP + r] = t;
+        }
+        __syncthreads();
+        if (threadIdx.x < R) {
+            float t = 0.f;
+            for (int w = 0; w < SK_THREADS / 32; ++w) t += wred[w * RP + threadIdx.x];
+            P->inv_rms_p[threadIdx.x] = 1.0f / sqrtf(t / (float)d + P->eps);
         }
         if (threadIdx.x == 0) P->sk_cnt[nrb] = 0;
     }

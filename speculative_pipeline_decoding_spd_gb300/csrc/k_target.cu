@@ -60,21 +60,8 @@ __device__ __forceinline__ const T *row_ptr(const Plan *__restrict__ P, const La
     return nullptr;
 }
 
-// x staging: rms-normalised residual times the norm gain (fixed-order block reduction).
-__device__ __forceinline__ void stage_norm(const float *__restrict__ x, const float *__restrict__ g, int d, float eps,
-                                           float *xs, float *red) {
-    float ss = 0.f;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) {
-        const float v = x[k];
-        ss = fmaf(v, v, ss);
-    }
-    ss = block_sum(ss, red);
-    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
-    for (int k = threadIdx.x; k < d; k += blockDim.x) xs[k] = (x[k] * inv) * g[k];
-}
-
 template <typename T, int EPI>
-__global__ void __launch_bounds__(GEMV_THREADS) k_target_gemv(const Plan *__restrict__ P, int round) {
+__global__ void __launch_bounds__(GEMV_THREADS, 2) k_target_gemv(const Plan *__restrict__ P, int round) {
     extern __shared__ __align__(16) float xs[];
     __shared__ StageList SL;
     __shared__ float red[GEMV_WARPS * RG + 33];
@@ -110,13 +97,10 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_target_gemv(const Plan *__rest
             stage_norm(P->X + (long long)slot * d, w.g1, d, P->eps, xs, red);
         else if (EPI == EPI_GATEUP)
             stage_norm(P->X + (long long)slot * d, w.g2, d, P->eps, xs, red);
-        else if (EPI == EPI_OPROJ) {
-            const float *a = P->ATT + (long long)s * P->q_rows;
-            for (int k = threadIdx.x; k < K; k += blockDim.x) xs[k] = a[k];
-        } else {
-            const float *u = P->U + (long long)s * P->F;
-            for (int k = threadIdx.x; k < K; k += blockDim.x) xs[k] = u[k];
-        }
+        else if (EPI == EPI_OPROJ)
+            stage_f4(P->ATT + (long long)s * P->q_rows, xs, K);
+        else
+            stage_f4(P->U + (long long)s * P->F, xs, K);
         __syncthreads();
 
         constexpr int GR = EPI == EPI_GATEUP ? RG / 2 : RG;   // output units per group
@@ -205,7 +189,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_target_gemv(const Plan *__rest
 // LM head for {target exit row, draft newest row}: logits = W_lm (rms(h) * g), the
 // argmax with the lowest id on ties.  Tied heads stream W_lm once for both rows.
 template <typename T, bool TIED>
-__global__ void __launch_bounds__(GEMV_THREADS) k_lm_head(const Plan *__restrict__ P) {
+__global__ void __launch_bounds__(GEMV_THREADS, 2) k_lm_head(const Plan *__restrict__ P) {
     extern __shared__ __align__(16) float xs[];   // [2][d]
     __shared__ float red[GEMV_WARPS * RG * 2 + 33];
     __shared__ int s_rows[2], s_done, s_last;
