@@ -223,6 +223,27 @@ int spd_read_buffer(spd_handle *h, int32_t which, int32_t index, size_t offset, 
  * last spd_prefill (config.timing must be 1).  Synchronises. */
 int spd_kernel_timing(spd_handle *h, double *total_ms_host, int64_t *launches_host);
 
+/* ---- standalone decode attention ------------------------------------------------------
+ * The attention of one decode token, as each pipeline stage runs it (machine review "The
+ * reading": every in-flight token attends to all earlier positions of its layer's KV
+ * cache): out[h] = softmax(q[h] . K[:, h/G]^T / sqrt(hd)) V[:, h/G] over positions
+ * 0..seq_len-1, G = Hq / Hkv.
+ *   q      device fp32 [Hq][hd] (already rotated by RoPE)
+ *   k, v   device [seq_len][Hkv][hd] in dtype (SPD_F32 or SPD_BF16) — the KV-cache layout
+ *   out    device fp32 [Hq][hd]
+ *   Hq / Hkv in {1, 2, 4, 8}; hd 64 or 128; 1 <= seq_len <= 16384; q, k, v, out 16-byte
+ *   aligned.  Split-K over 128-position chunks merged in chunk order (deterministic).
+ * spd_attention_scratch_bytes gives the scratch size; the scratch (device, 256-byte
+ * aligned, borrowed) needs no initialisation.  Work is queued on `stream`; the call does
+ * not synchronise.  Errors: SPD_EINVAL (shape, pointer, alignment), SPD_ENOMEM (scratch
+ * too small), SPD_ECUDA; text in spd_ops_last_error(). */
+int spd_attention_scratch_bytes(int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq_len, size_t *bytes);
+int spd_attention_decode(int32_t dtype, int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq_len, const float *q,
+                         const void *k, const void *v, float *out, void *scratch, size_t scratch_bytes, void *stream);
+
+/* Text of the calling thread's last failure of a standalone entry point ("" if none). */
+const char *spd_ops_last_error(void);
+
 /* Return to the post-create state (keeps weights and workspace). */
 int spd_reset(spd_handle *h);
 

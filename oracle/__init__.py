@@ -19,7 +19,7 @@ itself (closed forms, library routines, brute force, published known-answer valu
 except the draft-aware speedup model (the paper's Eqs. 10-12), whose formulas are not
 on the pages: parity unpinned, and not implemented.
 """
-from .model import Model, KVCache, rmsnorm, rope, silu, layer_block, argmax_fp32  # noqa: F401
+from .model import Model, KVCache, rmsnorm, rope, silu, layer_block, argmax_fp32, attend  # noqa: F401
 from .spd import (SPDOracle, Replay, ar_decode, stage_bounds, closed_form_alpha,  # noqa: F401
                   replay_decisions, TrackedCache)
 from . import philox, sampling  # noqa: F401

@@ -70,6 +70,28 @@ class Layer:
         self.g1 = to_f64(w["attn_norm"]); self.g2 = to_f64(w["ffn_norm"])
 
 
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, pos: np.ndarray) -> np.ndarray:
+    """Causal GQA attention: q [M][Hq][hd] at absolute positions pos[M], K/V [S][Hkv][hd]
+    for positions 0..S-1; row m sees positions <= pos[m].  softmax(q k^T / sqrt(hd)) v,
+    query head h reading kv head h // (Hq / Hkv)."""
+    M, Hq, hd = q.shape
+    S, Hkv = K.shape[0], K.shape[1]
+    group = Hq // Hkv
+    scale = 1.0 / np.sqrt(hd)
+    mask = np.asarray(pos)[:, None] >= np.arange(S)[None, :]           # [M][S]
+    out = np.empty((M, Hq, hd))
+    for h in range(Hq):
+        kh = K[:, h // group, :]
+        vh = V[:, h // group, :]
+        sc = (q[:, h, :] @ kh.T) * scale                             # [M][S]
+        sc = np.where(mask, sc, -np.inf)
+        sc = sc - sc.max(axis=1, keepdims=True)
+        p = np.exp(sc)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ vh
+    return out
+
+
 def layer_block(dm: ModelDims, W: Layer, H: np.ndarray, pos0: int, cache: KVCache, li: int,
                 reads: Optional[list] = None) -> np.ndarray:
     """One decoder layer over M consecutive positions pos0..pos0+M-1.
@@ -92,20 +114,7 @@ def layer_block(dm: ModelDims, W: Layer, H: np.ndarray, pos0: int, cache: KVCach
     S = pos0 + M
     if reads is not None:
         reads.append((li, 0, S - 1))
-    Kc, Vc = cache.K[li][:S], cache.V[li][:S]
-    group = dm.Hq // dm.Hkv
-    scale = 1.0 / np.sqrt(dm.hd)
-    mask = pos[:, None] >= np.arange(S)[None, :]                      # [M][S] causal
-    out = np.empty((M, dm.Hq, dm.hd))
-    for h in range(dm.Hq):
-        kh = Kc[:, h // group, :]
-        vh = Vc[:, h // group, :]
-        sc = (q[:, h, :] @ kh.T) * scale                             # [M][S]
-        sc = np.where(mask, sc, -np.inf)
-        sc = sc - sc.max(axis=1, keepdims=True)
-        p = np.exp(sc)
-        p = p / p.sum(axis=1, keepdims=True)
-        out[:, h, :] = p @ vh
+    out = attend(q, cache.K[li][:S], cache.V[li][:S], pos)
     H = H + out.reshape(M, dm.Hq * dm.hd) @ W.wo.T
     y = rmsnorm(H, W.g2, dm.rms_eps)
     u = silu(y @ W.wg.T) * (y @ W.wu.T)

@@ -81,6 +81,10 @@ SIGNATURES = [
     ("spd_get_tokens", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.POINTER(C.c_int32)]),
     ("spd_read_buffer", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_size_t, C.c_void_p, C.c_size_t]),
     ("spd_kernel_timing", C.c_int, [C.c_void_p, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
+    ("spd_attention_scratch_bytes", C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_size_t)]),
+    ("spd_attention_decode", C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    ("spd_ops_last_error", C.c_char_p, []),
     ("spd_reset", C.c_int, [C.c_void_p]),
     ("spd_destroy", None, [C.c_void_p]),
     ("spd_last_error", C.c_char_p, [C.c_void_p]),
@@ -177,6 +181,31 @@ def spd_kernel_timing(h):
     n = C.c_int64(0)
     check(load().spd_kernel_timing(h, C.byref(ms), C.byref(n)), h)
     return ms.value, n.value
+
+
+def check_op(rc: int):
+    if rc != SPD_OK:
+        msg = load().spd_ops_last_error()
+        raise SPDError(rc, msg.decode() if msg else "")
+    return rc
+
+
+def spd_attention_scratch_bytes(Hq: int, Hkv: int, hd: int, seq_len: int) -> int:
+    out = C.c_size_t(0)
+    check_op(load().spd_attention_scratch_bytes(Hq, Hkv, hd, seq_len, C.byref(out)))
+    return out.value
+
+
+def spd_attention_decode(dtype: int, Hq: int, Hkv: int, hd: int, seq_len: int, q_ptr: int, k_ptr: int, v_ptr: int,
+                         out_ptr: int, scratch_ptr: int, scratch_bytes: int, stream_ptr: int = 0):
+    check_op(load().spd_attention_decode(dtype, Hq, Hkv, hd, seq_len, C.c_void_p(q_ptr), C.c_void_p(k_ptr),
+                                         C.c_void_p(v_ptr), C.c_void_p(out_ptr), C.c_void_p(scratch_ptr),
+                                         C.c_size_t(scratch_bytes), C.c_void_p(stream_ptr)))
+
+
+def spd_ops_last_error() -> str:
+    m = load().spd_ops_last_error()
+    return m.decode() if m else ""
 
 
 def spd_reset(h):

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspd_gb300.so")
-SOURCES = ["api.cu", "k_target.cu", "k_attn.cu", "k_pdm.cu", "k_verify.cu", "k_prefill.cu"]
+SOURCES = ["api.cu", "k_target.cu", "k_attn.cu", "k_pdm.cu", "k_verify.cu", "k_prefill.cu", "k_ops.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--extended-lambda"]
 
@@ -37,7 +37,7 @@ def _stale(obj: str, deps) -> bool:
 def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(OUT, exist_ok=True)
     cc = nvcc()
-    header_deps = [os.path.join(CSRC, "common.cuh"), os.path.join(HERE, "..", "include", "spd.h")]
+    header_deps = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "attn.cuh"), os.path.join(HERE, "..", "include", "spd.h")]
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)

@@ -1,0 +1,100 @@
+// Standalone decode attention through the C ABI: the same kernel code the pipeline step
+// runs per stage (attn.cuh), on caller-given q, K and V.  Lets users (and the parity
+// tests) drive one attention problem without building a whole model handle.
+#include <cuda_runtime.h>
+
+#include <string>
+
+#include "attn.cuh"
+
+using namespace spd;
+
+namespace {
+thread_local std::string g_ops_error;
+
+int ops_fail(int code, const std::string &msg) {
+    g_ops_error = msg;
+    return code;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Bytes of split-K scratch one call needs: Hkv counters (256-byte padded), then the
+// [Hq][chunks][hd + 2] partials.
+size_t attn_scratch_bytes(int Hq, int Hkv, int hd, int seq_len) {
+    const int nch = (seq_len + ATT_CHUNK - 1) / ATT_CHUNK;
+    return align256((size_t)Hkv * sizeof(int)) + (size_t)Hq * nch * (hd + 2) * sizeof(float);
+}
+
+int attn_validate(int dtype, int Hq, int Hkv, int hd, int seq_len, const void *q, const void *k, const void *v,
+                  const void *out) {
+    if (dtype != SPD_F32 && dtype != SPD_BF16) return ops_fail(SPD_EINVAL, "dtype must be SPD_F32 or SPD_BF16");
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv) return ops_fail(SPD_EINVAL, "need Hq % Hkv == 0");
+    const int G = Hq / Hkv;
+    if (G > 8 || (G & (G - 1))) return ops_fail(SPD_EINVAL, "Hq / Hkv must be 1, 2, 4 or 8");
+    if (hd != 64 && hd != 128) return ops_fail(SPD_EINVAL, "head dim must be 64 or 128");
+    if (seq_len < 1 || seq_len > 16384) return ops_fail(SPD_EINVAL, "seq_len must be in [1, 16384]");
+    if (!q || !k || !v || !out) return ops_fail(SPD_EINVAL, "null pointer");
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(out)) % 16)
+        return ops_fail(SPD_EINVAL, "q, k, v and out must be 16-byte aligned");
+    return SPD_OK;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ATT_THREADS) k_attn_direct(AttnArgs<T> a) {
+    attn_cta<T>(a, blockIdx.x % a.Hkv, blockIdx.x / a.Hkv);
+}
+
+// Launch over (chunks x Hkv) CTAs with scratch = [counters | partials]; counters are
+// cleared on the stream first.
+int attn_launch(int dtype, int Hq, int Hkv, int hd, int seq_len, const float *q, const void *k, const void *v,
+                float *out, char *scratch, cudaStream_t s) {
+    const int nch = (seq_len + ATT_CHUNK - 1) / ATT_CHUNK;
+    int *cnt = reinterpret_cast<int *>(scratch);
+    float *part = reinterpret_cast<float *>(scratch + align256((size_t)Hkv * sizeof(int)));
+    cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)Hkv * sizeof(int), s);
+    if (e != cudaSuccess) return ops_fail(SPD_ECUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+    const dim3 grid(nch * Hkv);
+    if (dtype == SPD_BF16) {
+        AttnArgs<__nv_bfloat16> a{q, nullptr, nullptr, nullptr,
+                                  const_cast<__nv_bfloat16 *>(reinterpret_cast<const __nv_bfloat16 *>(k)),
+                                  const_cast<__nv_bfloat16 *>(reinterpret_cast<const __nv_bfloat16 *>(v)), seq_len,
+                                  out, part, cnt, 0, nch, Hq, Hkv, hd, 1.0f / sqrtf((float)hd)};
+        const int sm = att_smem_bytes<__nv_bfloat16>(hd);
+        cudaFuncSetAttribute(k_attn_direct<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+        k_attn_direct<__nv_bfloat16><<<grid, ATT_THREADS, sm, s>>>(a);
+    } else {
+        AttnArgs<float> a{q, nullptr, nullptr, nullptr, const_cast<float *>(reinterpret_cast<const float *>(k)),
+                          const_cast<float *>(reinterpret_cast<const float *>(v)), seq_len, out, part, cnt, 0, nch, Hq,
+                          Hkv, hd, 1.0f / sqrtf((float)hd)};
+        const int sm = att_smem_bytes<float>(hd);
+        cudaFuncSetAttribute(k_attn_direct<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+        k_attn_direct<float><<<grid, ATT_THREADS, sm, s>>>(a);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return ops_fail(SPD_ECUDA, std::string("attention launch: ") + cudaGetErrorString(e));
+    return SPD_OK;
+}
+}  // namespace
+
+extern "C" int spd_attention_scratch_bytes(int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq_len, size_t *bytes) {
+    if (!bytes) return ops_fail(SPD_EINVAL, "bytes is NULL");
+    if (Hq < 1 || Hkv < 1 || seq_len < 1 || (hd != 64 && hd != 128)) return ops_fail(SPD_EINVAL, "bad shape");
+    *bytes = attn_scratch_bytes(Hq, Hkv, hd, seq_len);
+    return SPD_OK;
+}
+
+extern "C" int spd_attention_decode(int32_t dtype, int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq_len,
+                                    const float *q, const void *k, const void *v, float *out, void *scratch,
+                                    size_t scratch_bytes, void *stream) {
+    int rc = attn_validate(dtype, Hq, Hkv, hd, seq_len, q, k, v, out);
+    if (rc) return rc;
+    if (!scratch || reinterpret_cast<uintptr_t>(scratch) % 256) return ops_fail(SPD_EINVAL, "scratch must be 256-byte aligned");
+    if (scratch_bytes < attn_scratch_bytes(Hq, Hkv, hd, seq_len))
+        return ops_fail(SPD_ENOMEM, "scratch too small: see spd_attention_scratch_bytes");
+    return attn_launch(dtype, Hq, Hkv, hd, seq_len, q, k, v, out, reinterpret_cast<char *>(scratch),
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" const char *spd_ops_last_error(void) { return g_ops_error.c_str(); }

@@ -152,3 +152,20 @@ def test_feature_masks_deeper_anchors():
     np.testing.assert_array_equal(m.feature(vals, 0), [1, 2, 3, 0, 0, 0, 0, 0, 0])
     np.testing.assert_array_equal(m.feature(vals, 3), [1, 2, 3, 4, 5, 6, 0, 0, 0])
     np.testing.assert_array_equal(m.feature(vals, 4), [1, 2, 3, 4, 5, 6, 7, 8, 9])
+
+
+@pytest.mark.parametrize("Hq,Hkv,S", [(4, 4, 1), (8, 2, 9), (8, 1, 33)])
+def test_attend_matches_torch_sdpa(Hq, Hkv, S):
+    """Single decode query (position S-1) against torch's scaled_dot_product_attention."""
+    from oracle import attend
+    rng = np.random.default_rng(S)
+    hd = 16
+    q = rng.normal(size=(1, Hq, hd))
+    K = rng.normal(size=(S, Hkv, hd))
+    V = rng.normal(size=(S, Hkv, hd))
+    out = attend(q, K, V, np.array([S - 1]))
+    t = torch.from_numpy
+    rep = Hq // Hkv
+    ref = F.scaled_dot_product_attention(t(q).permute(1, 0, 2), t(K).repeat_interleave(rep, 1).permute(1, 0, 2),
+                                         t(V).repeat_interleave(rep, 1).permute(1, 0, 2))
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12)
