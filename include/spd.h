@@ -241,6 +241,20 @@ int spd_attention_scratch_bytes(int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq
 int spd_attention_decode(int32_t dtype, int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq_len, const float *q,
                          const void *k, const void *v, float *out, void *scratch, size_t scratch_bytes, void *stream);
 
+/* Scratch-free spd_attention_decode (no counterpart in the paper; a library convenience).
+ * For callers that cannot lend device memory — all of theirs is owned by another
+ * allocator, or a cudaMalloc and its implicit synchronisation is not acceptable where
+ * they run.  Same arguments, result and errors as spd_attention_decode minus the
+ * scratch: the split-K partials live in a 1 MiB array inside the library, reserved on
+ * every GPU that loads it until the process exits (e.g. Hq 32, hd 128: seq_len up to
+ * 8064).  Larger shapes fail with SPD_ECAPACITY.  The entry point itself allocates
+ * nothing (no cudaMalloc / cudaFree).  Its first call on a device looks up the array's
+ * device address for that device (make that first call before any stream capture).
+ * Every call shares the array: each clears what must start at zero, and calls that
+ * overlap on the GPU (other streams, other threads) race and give wrong results. */
+int spd_attention_decode_noalloc(int32_t dtype, int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq_len,
+                                 const float *q, const void *k, const void *v, float *out, void *stream);
+
 /* Text of the calling thread's last failure of a standalone entry point ("" if none). */
 const char *spd_ops_last_error(void);
 

@@ -84,6 +84,8 @@ SIGNATURES = [
     ("spd_attention_scratch_bytes", C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_size_t)]),
     ("spd_attention_decode", C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    ("spd_attention_decode_noalloc", C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+                                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     ("spd_ops_last_error", C.c_char_p, []),
     ("spd_reset", C.c_int, [C.c_void_p]),
     ("spd_destroy", None, [C.c_void_p]),
@@ -201,6 +203,12 @@ def spd_attention_decode(dtype: int, Hq: int, Hkv: int, hd: int, seq_len: int, q
     check_op(load().spd_attention_decode(dtype, Hq, Hkv, hd, seq_len, C.c_void_p(q_ptr), C.c_void_p(k_ptr),
                                          C.c_void_p(v_ptr), C.c_void_p(out_ptr), C.c_void_p(scratch_ptr),
                                          C.c_size_t(scratch_bytes), C.c_void_p(stream_ptr)))
+
+
+def spd_attention_decode_noalloc(dtype: int, Hq: int, Hkv: int, hd: int, seq_len: int, q_ptr: int, k_ptr: int,
+                                 v_ptr: int, out_ptr: int, stream_ptr: int = 0):
+    check_op(load().spd_attention_decode_noalloc(dtype, Hq, Hkv, hd, seq_len, C.c_void_p(q_ptr), C.c_void_p(k_ptr),
+                                                 C.c_void_p(v_ptr), C.c_void_p(out_ptr), C.c_void_p(stream_ptr)))
 
 
 def spd_ops_last_error() -> str:

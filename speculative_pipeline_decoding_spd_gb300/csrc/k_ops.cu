@@ -3,6 +3,7 @@
 // tests) drive one attention problem without building a whole model handle.
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <string>
 
 #include "attn.cuh"
@@ -98,3 +99,55 @@ extern "C" int spd_attention_decode(int32_t dtype, int32_t Hq, int32_t Hkv, int3
 }
 
 extern "C" const char *spd_ops_last_error(void) { return g_ops_error.c_str(); }
+
+// ---------------------------------------------------------------------------------------
+// Scratch-free variant.  Some callers cannot hand out device memory: their allocations are
+// all owned by another allocator (a framework's caching allocator, a fixed arena) with no
+// spare buffer to lend, or they run where cudaMalloc's implicit device synchronisation is
+// not acceptable.  For them the split-K scratch lives in this file-scope array, reserved
+// on every GPU that loads the library until the process exits.  Calls share it: each call
+// clears the arrival counters it needs, the partials need no clearing, and two calls
+// that run at the same time on the GPU race on it.
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(1) << 20;   // 1 MiB
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of the array on the current device, looked up once per device.  In host
+// code the array's name is only a stand-in; the kernel must get this address.
+int noalloc_scratch(char **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return ops_fail(SPD_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return ops_fail(SPD_EINVAL, "device index above 63");
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return ops_fail(SPD_ECUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = reinterpret_cast<char *>(g_noalloc_ptr[dev]);
+    return SPD_OK;
+}
+}  // namespace
+
+extern "C" int spd_attention_decode_noalloc(int32_t dtype, int32_t Hq, int32_t Hkv, int32_t hd, int32_t seq_len,
+                                            const float *q, const void *k, const void *v, float *out, void *stream) {
+    int rc = attn_validate(dtype, Hq, Hkv, hd, seq_len, q, k, v, out);
+    if (rc) return rc;
+    const size_t need = attn_scratch_bytes(Hq, Hkv, hd, seq_len);
+    if (need > NOALLOC_SCRATCH_BYTES)
+        return ops_fail(SPD_ECAPACITY, "spd_attention_decode_noalloc: this shape needs " + std::to_string(need) +
+                                           " bytes of scratch, the built-in buffer holds " +
+                                           std::to_string(NOALLOC_SCRATCH_BYTES) +
+                                           "; use spd_attention_decode with caller scratch");
+    char *scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    return attn_launch(dtype, Hq, Hkv, hd, seq_len, q, k, v, out, scratch, reinterpret_cast<cudaStream_t>(stream));
+}
