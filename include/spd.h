@@ -84,7 +84,8 @@ typedef struct spd_target_weights {
     const void *lm_head;
 } spd_target_weights;
 
-/* Pipeline Draft Module ("Spec_theta + LM head", review "invented entities"):
+/* Pipeline Draft Module (a learned speculation network followed by an LM head; review
+ * "Assumptions & free parameters", invented entities):
  * proj [d][n_anchors*d] (one bias-free projection of the concatenated anchors),
  * Ls target-shaped layers (HOST array, copied), its own final_norm [d] fp32, and an
  * LM head [V][d] that may alias the target's (tied; the usual case). */

@@ -17,7 +17,7 @@ argument" and "Core claim"; page 2 referee report, comment on section 3.3, Eq. 3
   * an anchor h^(a) is the residual stream after a target layers (h^(0) = embedding);
   * a row's feature concatenates h^(a) over the anchor set B, with anchors deeper than
     the row's current depth replaced by zeros (in-flight tokens only have the
-    "deepest already-computed" checkpoints; the newest token only the embedding);
+    checkpoints they have already computed; the newest token only the embedding);
   * f = W_p feature (one bias-free projection), then Ls target-shaped decoder layers
     with their own weights and final norm, then the (tied) target LM head.
 """

@@ -6,7 +6,7 @@ schedule, ten rounds).
 Oracle-side implementation (test infrastructure).  The CUDA path carries its own,
 written independently from the same definition; the two are compared bit for bit.
 
-Stream layout used by the method (the pages only say "seeded Philox uniforms"):
+Stream layout used by the method (the pages only say the uniforms come from a seeded Philox):
 key = (seed & 0xffffffff, seed >> 32); counter = (step t, purpose, 0, 0).
 Purposes: 0 draft sample, 1 accept test, 2 target / residual sample,
 3 forced-draft coin, 4 forced-draft alternative id.  The prefill's first sample is t = 0.

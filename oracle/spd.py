@@ -25,7 +25,7 @@ Readings where the pages are silent or garbled:
     verification commits exactly one token (the kept draft or the correction), and no
     bonus token exists, so alpha = N / K <= 1 and the draft-free speedup S0 = alpha * n;
   * after a rejection the emptied stages do no work (bubbles exist, contrary to the
-    blog page's "zero bubbles");
+    blog page's claim that no stage idles);
   * generation stops as soon as 1 + N reaches max_new (y0 counts), in-flight tokens are
     discarded; no EOS (random weights).
 """

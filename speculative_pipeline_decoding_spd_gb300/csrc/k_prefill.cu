@@ -1,8 +1,8 @@
 // Prefill: the prompt's dense pass through all target layers, the draft module's cached
 // prefix, and the first token.  Not part of the timed step; it fills what the step
 // needs: every layer's K,V for the prompt positions and the draft module's K,V built
-// from full-depth anchor features of the verified prefix (machine review "What carries
-// the argument": "depth-maximized features for verified prefixes").
+// from full-depth anchor features of the verified prefix (machine review, "What carries
+// the argument": verified positions use every anchor depth).
 //
 // The prompt is processed in chunks of pf_rows positions (each chunk attends causally to
 // the cache of the chunks before it), with an fp32 tiled CUDA-core GEMM (weights bf16 or

@@ -10,7 +10,7 @@
 // the draft x with probability min(1, p_T(x) / p_D(x)), else draw from the normalised
 // residual max(0, p_T - p_D).
 //
-// Philox stream (the pages only say "seeded Philox uniforms"): counter (t, purpose),
+// Philox stream (the pages only say the uniforms come from a seeded Philox): counter (t, purpose),
 // purposes 0 draft sample, 1 keep test, 2 target / residual sample, 3 forced coin,
 // 4 forced alternative id; u = (word >> 8) * 2^-24.
 #include "common.cuh"
