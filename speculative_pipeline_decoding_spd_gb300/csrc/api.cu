@@ -126,7 +126,7 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.X = b.take<float>((size_t)ns * d->d);
     h.QKV = b.take<float>((size_t)n * qkv);
     h.ATT = b.take<float>((size_t)n * qr);
-    h.U = b.take<float>((size_t)n * d->F);
+    h.U = b.take<float>((size_t)n * 2 * d->F);
     h.ANCH = b.take<float>((size_t)ns * c->n_anchors * d->d);
     h.kc = b.take<char>((size_t)d->L * kvs * elem);
     h.vc = b.take<char>((size_t)d->L * kvs * elem);

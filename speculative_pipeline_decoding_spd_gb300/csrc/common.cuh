@@ -8,7 +8,7 @@
 //   ANCH fp32 [n+1][nB][d]       anchor states per slot (depth a = after a layers, 0 = embedding)
 //   QKV fp32 [n][(Hq+2Hkv) hd]   raw q,k,v of each stage (RoPE is applied by the attention kernel)
 //   ATT fp32 [n][Hq hd]          attention output of each stage
-//   U   fp32 [n][F]              silu(gate) * up of each stage
+//   U   fp32 [n][2F]             raw gate and up sums of each stage (SiLU(gate)*up formed by the down GEMV)
 //   K/V cache per target layer   dtype [max_seq][Hkv][hd]; valid length per layer in DevState
 //   draft module buffers         Xp [n+1][d], QKVp/ATTp/GUp per row, its own K/V cache
 //   logits fp32 [2][V]           row 0 = target prediction of the exiting token, row 1 = draft
@@ -39,6 +39,7 @@ constexpr int ERR_TRACE_FULL = 2;
 constexpr int ERR_SEQ_FULL = 3;
 constexpr int ERR_ROWS = 4;
 constexpr int ERR_TOKEN = 5;
+constexpr int ERR_TIMEOUT = 6;   // a bounded mbarrier wait gave up
 
 struct LayerW {
     const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
@@ -78,7 +79,7 @@ struct Plan {
     LayerW tl[MAXL];
     LayerW pl[MAXPL];
     // workspace
-    float *X, *QKV, *ATT, *U, *ANCH;
+    float *X, *QKV, *ATT, *U, *ANCH;   // U: [n][2F] gate | up
     void *kc, *vc, *pkc, *pvc;
     long long kv_stride;           // elements per layer cache
     float2 *rope;                  // [max_seq][hd/2] (cos, sin)
@@ -106,6 +107,56 @@ struct Plan {
     float *pf_logits;              // [V]
     Plan *self;                    // device address of this plan
 };
+
+// ---------------------------------------------------------------------------------
+// mbarrier + 1-D bulk copy (TMA) helpers.  Every wait is bounded in time: on timeout the
+// caller records an error flag and carries on (no trap, no endless spin).
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
+// Wait for the completion of the phase with this parity; false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+    return true;
+}
+// 1-D bulk copy global -> this CTA's shared memory; completion counted in bytes on bar.
+// src, dst and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+// Barrier among the first `threads` threads of the CTA (id 0 is __syncthreads').
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // ---------------------------------------------------------------------------------
 // element access

@@ -22,6 +22,9 @@ SMALL = Case(si.ModelDims(L=6, d=256, Hq=4, Hkv=2, hd=64, F=512, V=2000), n=3, a
 # bf16, hd 128, GQA 4 (the 4B shape's head layout), 5 layers over 4 stages (ragged stages)
 HD128 = Case(si.ModelDims(L=5, d=512, Hq=8, Hkv=2, hd=128, F=1024, V=3000), n=4, anchors=(0, 2, 5), Ls=1,
              prompt_len=140, max_new=40, norms="perturbed")
+# bf16, rows longer than one 4 KB tile chunk (d 2560, F 2304: two K chunks per row)
+MULTI = Case(si.ModelDims(L=4, d=2560, Hq=8, Hkv=2, hd=128, F=2304, V=1000), n=3, anchors=(0, 2, 4), Ls=1,
+             prompt_len=200, max_new=40, norms="perturbed")
 
 
 def _prefill_logits_close(case, pf):
@@ -35,13 +38,13 @@ def _prefill_logits_close(case, pf):
     return err
 
 
-@pytest.mark.parametrize("case", [TINY, SMALL, HD128], ids=["tiny", "small", "hd128"])
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI], ids=["tiny", "small", "hd128", "multi"])
 def test_prefill_logits(case):
     toks, tr, st, pf = run_gpu(case, force_p=1.0, forced_ref=torch.zeros(case.max_seq, dtype=torch.int32).cuda())
     _prefill_logits_close(case, pf)
 
 
-@pytest.mark.parametrize("case", [TINY, SMALL, HD128], ids=["tiny", "small", "hd128"])
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI], ids=["tiny", "small", "hd128", "multi"])
 def test_greedy_draft_module_replay(case):
     toks, tr, st, pf = run_gpu(case)
     o, rep = replay_oracle(case, tr, toks)
@@ -50,8 +53,8 @@ def test_greedy_draft_module_replay(case):
     assert st["N"] == case.max_new - 1 and st["K"] == len(tr)
 
 
-@pytest.mark.parametrize("case,p", [(TINY, 0.6), (SMALL, 0.5), (SMALL, 0.9), (HD128, 0.7)],
-                         ids=["tiny-0.6", "small-0.5", "small-0.9", "hd128-0.7"])
+@pytest.mark.parametrize("case,p", [(TINY, 0.6), (SMALL, 0.5), (SMALL, 0.9), (HD128, 0.7), (MULTI, 0.6)],
+                         ids=["tiny-0.6", "small-0.5", "small-0.9", "hd128-0.7", "multi-0.6"])
 def test_forced_draft_replay(case, p):
     ar = ar_reference(case)
     tg, pd, prompt, m, _, _ = materialise(case)
@@ -63,7 +66,7 @@ def test_forced_draft_replay(case, p):
     assert st["accepts"] > 0 and st["rejects"] > 0
 
 
-@pytest.mark.parametrize("case", [TINY, SMALL, HD128], ids=["tiny", "small", "hd128"])
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI], ids=["tiny", "small", "hd128", "multi"])
 def test_pipeline_equals_single_stage_bitwise(case):
     """Losslessness on the device: for every n the pipelined decode commits the same
     tokens as n = 1 (one token through all layers per step), and the per-step target
