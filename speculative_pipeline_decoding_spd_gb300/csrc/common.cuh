@@ -131,18 +131,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
-// Wait for the completion of the phase with this parity; false after WAIT_LIMIT_NS.
+constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;   // ~2 s of SM clock: far beyond any legitimate wait
+// Wait for the completion of the phase with this parity; false after WAIT_LIMIT_CYCLES.
+// The bound uses the SM's own cycle counter, which is cheap to read inside the spin.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
     return true;
 }
 // 1-D bulk copy global -> this CTA's shared memory; completion counted in bytes on bar.
@@ -344,30 +340,82 @@ __device__ __forceinline__ uint32_t philox_word0(uint32_t t, uint32_t purpose, u
 // tokens oldest first; consecutive positions pos0, pos0+1, ...
 struct PdmRows {
     int R, pos0;
-    int slot[MAXS], depth[MAXS];
+    int slot[MAXS], depth[MAXS], pos[MAXS];
 };
 
-__device__ __forceinline__ void build_pdm_rows(const Plan *__restrict__ P, PdmRows &pr) {
+// Occupied stages that have a layer at this round, in stage order.
+struct StageList {
+    int m;
+    int stage[MAXS], slot[MAXS], layer[MAXS], pos[MAXS];
+};
+
+// Both are built by one full warp (lane s looks at stage s, so the slot-ring reads of all
+// stages are in flight together).  Only the calling warp sees the result until the CTA
+// synchronises.
+__device__ __forceinline__ void warp_stage_list(const Plan *__restrict__ P, int round, StageList &L, int *done) {
+    const int lane = threadIdx.x & 31;
     const DevState *st = P->st;
-    const int n = P->n, ns = n + 1, head = st->head;
-    int R = 0, pos0 = 0;
-    if (st->pending) {
-        const int slot = ring(head, n, ns);
+    const int n = P->n, head = st->head;
+    bool ok = false;
+    int slot = 0, layer = 0, pos = 0;
+    if (lane < n) {
+        slot = ring(head, lane, n + 1);
+        const int v = st->valid[slot];
+        const int b0 = P->b[lane], b1 = P->b[lane + 1];
+        pos = st->pos[slot];
+        layer = b0 + round;
+        ok = v && layer < b1;
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, ok);
+    if (ok) {
+        const int i = __popc(mask & ((1u << lane) - 1u));
+        L.stage[i] = lane;
+        L.slot[i] = slot;
+        L.layer[i] = layer;
+        L.pos[i] = pos;
+    }
+    if (lane == 0) {
+        L.m = __popc(mask);
+        if (done) *done = st->done;
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ void warp_pdm_rows(const Plan *__restrict__ P, PdmRows &pr, int *done) {
+    const int lane = threadIdx.x & 31;
+    const DevState *st = P->st;
+    const int n = P->n, head = st->head, pending = st->pending;
+    bool v = false;
+    int slot = 0, pos = 0, depth = 0;
+    if (lane < n) {
+        slot = ring(head, lane, n + 1);
+        v = st->valid[slot] != 0;
+        pos = st->pos[slot];
+        depth = P->b[lane];
+    } else if (lane == n && pending) {
+        slot = ring(head, n, n + 1);
+        pos = st->pos[slot];
+        depth = P->L;
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, v);
+    if (v) {
+        // rows: exited token first, then stages from the deepest (oldest) to stage 0
+        const int i = (pending ? 1 : 0) + __popc(lane == 31 ? 0u : (mask >> (lane + 1)));
+        pr.slot[i] = slot;
+        pr.depth[i] = depth;
+        pr.pos[i] = pos;
+    } else if (lane == n && pending) {
         pr.slot[0] = slot;
-        pr.depth[0] = P->L;
-        pos0 = st->pos[slot];
-        R = 1;
+        pr.depth[0] = depth;
+        pr.pos[0] = pos;
     }
-    for (int s = n - 1; s >= 0; --s) {
-        const int slot = ring(head, s, ns);
-        if (!st->valid[slot]) continue;
-        if (R == 0) pos0 = st->pos[slot];
-        pr.slot[R] = slot;
-        pr.depth[R] = P->b[s];
-        ++R;
+    __syncwarp();
+    if (lane == 0) {
+        pr.R = (pending ? 1 : 0) + __popc(mask);
+        pr.pos0 = pr.R > 0 ? pr.pos[0] : 0;
+        if (done) *done = st->done;
     }
-    pr.R = R;
-    pr.pos0 = pos0;
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------------

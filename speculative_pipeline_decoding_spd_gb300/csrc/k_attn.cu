@@ -21,40 +21,33 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const Plan *__restrict__ P
     __shared__ int s_ok, s_pos, s_layer, s_src;
     const int Hkv = P->Hkv, hd = P->hd;
     const int g = blockIdx.x % Hkv, c = blockIdx.x / Hkv, prob = blockIdx.y;
-    const DevState *st = P->st;
-    if (threadIdx.x == 0) {
-        int ok = !st->done;
-        int pos = 0, layer = 0, src = 0;
-        if (ok && TARGET) {
-            const int n = P->n, ns = n + 1, head = st->head;
-            int m = 0;
-            ok = 0;
-            for (int s = 0; s < n; ++s) {
-                const int slot = ring(head, s, ns);
-                if (!st->valid[slot]) continue;
-                const int l = P->b[s] + arg;
-                if (l >= P->b[s + 1]) continue;
-                if (m == prob) {
-                    ok = 1;
-                    pos = st->pos[slot];
-                    layer = l;
-                    src = s;
-                }
-                ++m;
+    if (threadIdx.x < 32) {
+        __shared__ StageList SL;
+        __shared__ PdmRows PR;
+        __shared__ int s_dn;
+        int ok, pos = 0, layer = 0, src = 0;
+        if (TARGET) {
+            warp_stage_list(P, arg, SL, &s_dn);
+            ok = !s_dn && prob < SL.m;
+            if (ok) {
+                pos = SL.pos[prob];
+                layer = SL.layer[prob];
+                src = SL.stage[prob];
             }
-        } else if (ok) {
-            PdmRows pr;
-            build_pdm_rows(P, pr);
-            ok = prob < pr.R;
-            pos = pr.pos0 + prob;
+        } else {
+            warp_pdm_rows(P, PR, &s_dn);
+            ok = !s_dn && prob < PR.R;
+            pos = PR.pos0 + prob;
             layer = arg;
             src = prob;
         }
         if (ok && c * ATT_CHUNK > pos) ok = 0;
-        s_ok = ok;
-        s_pos = pos;
-        s_layer = layer;
-        s_src = src;
+        if (threadIdx.x == 0) {
+            s_ok = ok;
+            s_pos = pos;
+            s_layer = layer;
+            s_src = src;
+        }
     }
     __syncthreads();
     if (!s_ok) return;

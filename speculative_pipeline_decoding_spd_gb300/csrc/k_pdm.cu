@@ -82,10 +82,7 @@ __global__ void __launch_bounds__(SK_THREADS) k_skinny(const Plan *__restrict__ 
     extern __shared__ __align__(16) unsigned char sk_smem[];
     __shared__ PdmRows pr;
     __shared__ int s_done, s_last, s_glast;
-    if (threadIdx.x == 0) {
-        s_done = P->st->done;
-        build_pdm_rows(P, pr);
-    }
+    if (threadIdx.x < 32) warp_pdm_rows(P, pr, &s_done);
     __syncthreads();
     if (s_done) return;
     const int R = pr.R;

@@ -9,8 +9,9 @@
 // (stages x output rows) are spread evenly over the CTAs, so a partly filled pipeline
 // (after a flush) still streams its weights with the whole GPU.
 //
-// One CTA per SM: a producer warp streams weight tiles (8 rows x up to 4 KB of each row)
-// with 1-D bulk copies (TMA) into a 4-stage shared-memory ring, signalled by mbarriers;
+// One CTA per SM: a producer warp streams weight tiles (8 rows x up to 6 KB of each row)
+// with 1-D bulk copies (TMA) into a shared-memory ring of as many stages as fit beside x
+// (5 x 40 KB for the 4B shape's QKV and gate/up), signalled by mbarriers;
 // 8 consumer warps stage the input vector x (RMS-normalised where the layer needs it)
 // while the first tiles are already in flight; then warp q owns row q of every tile of a
 // group across all its K chunks, so a row ends with one warp shuffle tree and no CTA
@@ -28,35 +29,20 @@ enum { EPI_QKV = 0, EPI_OPROJ = 1, EPI_GATEUP = 2, EPI_DOWN = 3, EPI_LM = 4 };
 constexpr int TG_CONSUMERS = 256;               // 8 consumer warps
 constexpr int TG_THREADS = TG_CONSUMERS + 32;   // + 1 producer warp
 constexpr int TG_RG = 8;                        // weight rows per tile
-constexpr int TG_ROWB = 4096;                   // bytes of one row's chunk in a tile
-constexpr int TG_NS = 4;                        // ring stages
-constexpr int TG_STAGE = TG_RG * TG_ROWB;       // 32 KB
+constexpr int TG_ROWB = 6144;                   // at most this many bytes of a row per tile chunk
+constexpr int TG_MAXNS = 8;                     // ring stages (the ring fills what x leaves free)
+constexpr int TG_SMEM = 210 * 1024;             // dynamic shared memory: ring + x
 constexpr int BAR_C = 1;                        // named barrier of the consumer warps
 
-struct StageList {
-    int m;
-    int stage[MAXS], slot[MAXS], layer[MAXS];
-};
-
-// Occupied stages that have a layer at this round.
-__device__ void build_stage_list(const Plan *__restrict__ P, int round, StageList &L) {
-    const DevState *st = P->st;
-    const int n = P->n, ns = n + 1, head = st->head;
-    int m = 0;
-    for (int s = 0; s < n; ++s) {
-        const int slot = ring(head, s, ns);
-        if (!st->valid[slot]) continue;
-        const int layer = P->b[s] + round;
-        if (layer >= P->b[s + 1]) continue;
-        L.stage[m] = s;
-        L.slot[m] = slot;
-        L.layer[m] = layer;
-        ++m;
-    }
-    L.m = m;
-}
-
 // ---- consumer-only (256-thread) staging helpers: loads batched, named barrier --------
+// For bf16 weights x is kept in shared memory as two planes, element 8v+j at
+// xp(8v+j) = (j < 4 ? 0 : plane) + 4v + (j & 3), so the 16-byte x reads of a warp (lane v)
+// are contiguous per plane and hit distinct banks.
+template <typename T> __device__ __forceinline__ int xp(int k, int plane);
+template <> __device__ __forceinline__ int xp<float>(int k, int) { return k; }
+template <> __device__ __forceinline__ int xp<__nv_bfloat16>(int k, int plane) {
+    return ((k & 4) ? plane : 0) + ((k >> 3) << 2) + (k & 3);
+}
 __device__ __forceinline__ float c_block_sum(float v, float *red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_sum(v);
@@ -69,10 +55,10 @@ __device__ __forceinline__ float c_block_sum(float v, float *red) {
     return s;
 }
 
-__device__ __forceinline__ void c_stage_f4(const float *__restrict__ src, float *dst, int n) {
-    const int n4 = n >> 2;
+template <typename T>
+__device__ __noinline__ void c_stage_f4(const float *__restrict__ src, float *dst, int n) {
+    const int n4 = n >> 2, plane = n >> 1;
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
-    float4 *d4 = reinterpret_cast<float4 *>(dst);
     for (int b = threadIdx.x; b < n4; b += 8 * TG_CONSUMERS) {
         float4 v[8];
 #pragma unroll
@@ -83,17 +69,17 @@ __device__ __forceinline__ void c_stage_f4(const float *__restrict__ src, float 
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int i = b + u * TG_CONSUMERS;
-            if (i < n4) d4[i] = v[u];
+            if (i < n4) *reinterpret_cast<float4 *>(dst + xp<T>(4 * i, plane)) = v[u];
         }
     }
 }
 
 // xs[k] = silu(gu[k]) * gu[F + k] (gate and up sums of the previous kernel)
-__device__ __forceinline__ void c_stage_swiglu(const float *__restrict__ gu, float *xs, int F) {
-    const int n4 = F >> 2;
+template <typename T>
+__device__ __noinline__ void c_stage_swiglu(const float *__restrict__ gu, float *xs, int F) {
+    const int n4 = F >> 2, plane = F >> 1;
     const float4 *g4 = reinterpret_cast<const float4 *>(gu);
     const float4 *u4 = reinterpret_cast<const float4 *>(gu + F);
-    float4 *d4 = reinterpret_cast<float4 *>(xs);
     for (int b = threadIdx.x; b < n4; b += 4 * TG_CONSUMERS) {
         float4 gv[4], uv[4];
 #pragma unroll
@@ -108,24 +94,29 @@ __device__ __forceinline__ void c_stage_swiglu(const float *__restrict__ gu, flo
         for (int u = 0; u < 4; ++u) {
             const int i = b + u * TG_CONSUMERS;
             if (i < n4)
-                d4[i] = make_float4(silu_f(gv[u].x) * uv[u].x, silu_f(gv[u].y) * uv[u].y, silu_f(gv[u].z) * uv[u].z,
-                                    silu_f(gv[u].w) * uv[u].w);
+                *reinterpret_cast<float4 *>(xs + xp<T>(4 * i, plane)) =
+                    make_float4(silu_f(gv[u].x) * uv[u].x, silu_f(gv[u].y) * uv[u].y, silu_f(gv[u].z) * uv[u].z,
+                                silu_f(gv[u].w) * uv[u].w);
         }
     }
 }
 
 // xs = rms(x) * g over d (x staged first, fixed-order reduction); ends with a barrier
-__device__ void c_stage_norm(const float *__restrict__ x, const float *__restrict__ g, int d, float eps, float *xs,
+template <typename T>
+__device__ __noinline__ void c_stage_norm(const float *__restrict__ x, const float *__restrict__ g, int d, float eps, float *xs,
                              float *red) {
-    c_stage_f4(x, xs, d);
+    c_stage_f4<T>(x, xs, d);
     named_sync(BAR_C, TG_CONSUMERS);
+    const int plane = d >> 1;
     float ss = 0.f;
-    for (int k = threadIdx.x; k < d; k += TG_CONSUMERS) ss = fmaf(xs[k], xs[k], ss);
+    for (int k = threadIdx.x; k < d; k += TG_CONSUMERS) {
+        const float v = xs[xp<T>(k, plane)];
+        ss = fmaf(v, v, ss);
+    }
     ss = c_block_sum(ss, red);
     const float inv = 1.0f / sqrtf(ss / (float)d + eps);
     const int d4 = d >> 2;
     const float4 *g4 = reinterpret_cast<const float4 *>(g);
-    float4 *x4 = reinterpret_cast<float4 *>(xs);
     for (int b = threadIdx.x; b < d4; b += 8 * TG_CONSUMERS) {
         float4 gv[8];
 #pragma unroll
@@ -137,38 +128,92 @@ __device__ void c_stage_norm(const float *__restrict__ x, const float *__restric
         for (int u = 0; u < 8; ++u) {
             const int i = b + u * TG_CONSUMERS;
             if (i < d4) {
-                float4 v = x4[i];
+                float4 *px = reinterpret_cast<float4 *>(xs + xp<T>(4 * i, plane));
+                float4 v = *px;
                 v.x = (v.x * inv) * gv[u].x;
                 v.y = (v.y * inv) * gv[u].y;
                 v.z = (v.z * inv) * gv[u].z;
                 v.w = (v.w * inv) * gv[u].w;
-                x4[i] = v;
+                *px = v;
             }
         }
     }
     named_sync(BAR_C, TG_CONSUMERS);
 }
 
-// Weight row pointer of tile row q of the group starting at unit g0 (nullptr: no row).
-template <typename T, int EPI, bool TIED>
-__device__ __forceinline__ const T *tile_row(const Plan *__restrict__ P, const LayerW &w, int g0, int q, int r1, int K) {
-    if (EPI == EPI_GATEUP || (EPI == EPI_LM && !TIED)) {
-        const int u = g0 + (q & 3);
-        if (u >= r1) return nullptr;
-        const void *base;
-        if (EPI == EPI_GATEUP) base = q < 4 ? w.wg : w.wu;
-        else base = q < 4 ? P->lm_head : P->pdm_lm_head;
-        return reinterpret_cast<const T *>(base) + (long long)u * K;
-    }
-    const int r = g0 + q;
-    if (r >= r1) return nullptr;
-    if (EPI == EPI_LM) return reinterpret_cast<const T *>(P->lm_head) + (long long)r * K;
-    if (EPI == EPI_OPROJ) return reinterpret_cast<const T *>(w.wo) + (long long)r * K;
-    if (EPI == EPI_DOWN) return reinterpret_cast<const T *>(w.wd) + (long long)r * K;
-    if (r < P->q_rows) return reinterpret_cast<const T *>(w.wq) + (long long)r * K;
-    if (r < P->q_rows + P->kv_rows) return reinterpret_cast<const T *>(w.wk) + (long long)(r - P->q_rows) * K;
-    return reinterpret_cast<const T *>(w.wv) + (long long)(r - P->q_rows - P->kv_rows) * K;
+// One 16-byte weight vector (elements e..e+VEC-1) against x in its shared-memory layout.
+template <typename T>
+__device__ __forceinline__ float dot_x(const uint4 &w, const float *x, int e, int plane, float acc);
+template <>
+__device__ __forceinline__ float dot_x<float>(const uint4 &w, const float *x, int e, int, float acc) {
+    return dot16(w, x + e, acc, 0.f);
 }
+template <>
+__device__ __forceinline__ float dot_x<__nv_bfloat16>(const uint4 &w, const float *x, int e, int plane, float acc) {
+    const float4 a = *reinterpret_cast<const float4 *>(x + (e >> 1));
+    const float4 b = *reinterpret_cast<const float4 *>(x + plane + (e >> 1));
+    acc = fmaf(bf_lo(w.x), a.x, acc);
+    acc = fmaf(bf_hi(w.x), a.y, acc);
+    acc = fmaf(bf_lo(w.y), a.z, acc);
+    acc = fmaf(bf_hi(w.y), a.w, acc);
+    acc = fmaf(bf_lo(w.z), b.x, acc);
+    acc = fmaf(bf_hi(w.z), b.y, acc);
+    acc = fmaf(bf_lo(w.w), b.z, acc);
+    acc = fmaf(bf_hi(w.w), b.w, acc);
+    return acc;
+}
+
+// Weight rows of one problem, resolved once per segment into registers: unit u reads row
+// u of region 0 below b1, row u - b1 of region 1 below b2, else row u - b2 of region 2.
+// Gate/up and untied-head tiles read slot q < 4 from region 0 and q >= 4 from region 1
+// for the same unit.
+template <typename T>
+struct SegRows {
+    const T *p0, *p1, *p2;
+    int b1, b2;
+};
+
+template <typename T, int EPI, bool TIED>
+__device__ __forceinline__ SegRows<T> seg_rows(const Plan *__restrict__ P, const LayerW &w) {
+    SegRows<T> r;
+    r.b1 = r.b2 = 0x7fffffff;
+    if (EPI == EPI_GATEUP) {
+        r.p0 = reinterpret_cast<const T *>(w.wg);
+        r.p1 = reinterpret_cast<const T *>(w.wu);
+        r.p2 = nullptr;
+    } else if (EPI == EPI_LM) {
+        r.p0 = reinterpret_cast<const T *>(P->lm_head);
+        r.p1 = reinterpret_cast<const T *>(P->pdm_lm_head);
+        r.p2 = nullptr;
+    } else if (EPI == EPI_OPROJ || EPI == EPI_DOWN) {
+        r.p0 = reinterpret_cast<const T *>(EPI == EPI_OPROJ ? w.wo : w.wd);
+        r.p1 = r.p2 = nullptr;
+    } else {
+        r.p0 = reinterpret_cast<const T *>(w.wq);
+        r.p1 = reinterpret_cast<const T *>(w.wk);
+        r.p2 = reinterpret_cast<const T *>(w.wv);
+        r.b1 = P->q_rows;
+        r.b2 = P->q_rows + P->kv_rows;
+    }
+    return r;
+}
+
+template <typename T, int EPI, bool TIED>
+__device__ __forceinline__ const T *tile_row(const SegRows<T> &sr, int u, int q, int r1, int K) {
+    if (u >= r1) return nullptr;
+    if (EPI == EPI_GATEUP || (EPI == EPI_LM && !TIED)) return (q < 4 ? sr.p0 : sr.p1) + (long long)u * K;
+    if (EPI == EPI_QKV) {
+        if (u < sr.b1) return sr.p0 + (long long)u * K;
+        if (u < sr.b2) return sr.p1 + (long long)(u - sr.b1) * K;
+        return sr.p2 + (long long)(u - sr.b2) * K;
+    }
+    return sr.p0 + (long long)u * K;
+}
+
+// Units of a CTA's range [r0, r1) are spread over the tile slots: slot q of group g holds
+// unit r0 + (q mod GR) * per + g, per = ceil((r1 - r0) / GR), so the 8 copies of a tile
+// come from 8 places far apart in memory instead of one contiguous span.
+__device__ __forceinline__ int slot_unit(int r0, int per, int GR, int q, int g) { return r0 + (q % GR) * per + g; }
 
 template <typename T, int EPI, bool TIED>
 __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__ P, int round) {
@@ -177,9 +222,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
     constexpr int VEC = WTraits<T>::VEC;
     // units per tile group: rows, or (gate, up) / (head 0, head 1) row pairs
     constexpr int GR = (EPI == EPI_GATEUP || (EPI == EPI_LM && !TIED)) ? TG_RG / 2 : TG_RG;
-    unsigned char *stages = tg_smem;
-    float *xs = reinterpret_cast<float *>(tg_smem + TG_NS * TG_STAGE);
-    __shared__ __align__(8) uint64_t full[TG_NS], empty[TG_NS];
+    __shared__ __align__(8) uint64_t full[TG_MAXNS], empty[TG_MAXNS];
     __shared__ StageList SL;
     __shared__ float cred[TG_CONSUMERS / 32];
     __shared__ int s_done, s_rows[2], s_last;
@@ -187,24 +230,29 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
     __shared__ int s_bi[2][TG_CONSUMERS / 32];
     const DevState *st = P->st;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
-        s_done = st->done;
+    if (warp == 0) {
         if (EPI == EPI_LM) {
+            // exit slot (stage n-1 occupied?) and the draft module's newest row
             const int n = P->n, ns = n + 1, head = st->head;
-            s_rows[0] = st->valid[ring(head, n - 1, ns)] ? ring(head, n - 1, ns) : -1;   // exit slot
-            int R = st->pending ? 1 : 0;
-            for (int s = 0; s < n; ++s) R += st->valid[ring(head, s, ns)] ? 1 : 0;
-            s_rows[1] = R - 1;                                                          // newest draft row
-            SL.m = 1;
-            SL.stage[0] = SL.slot[0] = SL.layer[0] = 0;
+            const bool v = lane < n && st->valid[ring(head, lane, ns)] != 0;
+            const unsigned mask = __ballot_sync(0xffffffffu, v);
+            if (lane == 0) {
+                s_done = st->done;
+                s_rows[0] = (mask >> (n - 1)) & 1u ? ring(head, n - 1, ns) : -1;
+                s_rows[1] = (st->pending ? 1 : 0) + __popc(mask) - 1;
+                SL.m = 1;
+                SL.stage[0] = SL.slot[0] = SL.layer[0] = 0;
+            }
         } else {
-            build_stage_list(P, round, SL);
+            warp_stage_list(P, round, SL, &s_done);
         }
-        for (int i = 0; i < TG_NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], TG_CONSUMERS / 32);
+        if (lane == 0) {
+            for (int i = 0; i < TG_MAXNS; ++i) {
+                mbar_init(&full[i], 1);
+                mbar_init(&empty[i], TG_CONSUMERS / 32);
+            }
+            fence_mbar_init();
         }
-        fence_mbar_init();
     }
     __syncthreads();
     if (s_done || SL.m == 0) return;
@@ -214,6 +262,13 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
     const int K = (EPI == EPI_QKV || EPI == EPI_GATEUP || EPI == EPI_LM) ? d : (EPI == EPI_OPROJ ? P->q_rows : P->F);
     const int nch = (int)(((long long)K * sizeof(T) + TG_ROWB - 1) / TG_ROWB);
     const int KC = ((K + nch - 1) / nch + VEC - 1) / VEC * VEC;
+    // shared memory: x (NRHS x K floats) first, then the ring of 8-row tiles
+    const int xbytes = ((NRHS * K * (int)sizeof(float)) + 127) / 128 * 128;
+    const int rowb = (KC * (int)sizeof(T) + 127) / 128 * 128;
+    const int stage_bytes = TG_RG * rowb;
+    const int NS = min(TG_MAXNS, (TG_SMEM - xbytes) / stage_bytes);
+    float *xs = reinterpret_cast<float *>(tg_smem);
+    unsigned char *stages = tg_smem + xbytes;
     const long long total = (long long)SL.m * N;
     const long long lo = total * blockIdx.x / gridDim.x;
     const long long hi = total * (blockIdx.x + 1) / gridDim.x;
@@ -226,25 +281,26 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                 const int i = (int)(r / N);
                 const int r0 = (int)(r - (long long)i * N);
                 const int r1 = (int)min((long long)N, hi - (long long)i * N);
-                const LayerW &w = P->tl[SL.layer[i]];
-                for (int g0 = r0; g0 < r1; g0 += GR) {
+                const SegRows<T> sr = seg_rows<T, EPI, TIED>(P, P->tl[SL.layer[i]]);
+                const int per = (r1 - r0 + GR - 1) / GR;
+                for (int g = 0; g < per; ++g) {
                     const T *rp[TG_RG];
                     int nrows = 0;
 #pragma unroll
                     for (int q = 0; q < TG_RG; ++q) {
-                        rp[q] = tile_row<T, EPI, TIED>(P, w, g0, q, r1, K);
+                        rp[q] = tile_row<T, EPI, TIED>(sr, slot_unit(r0, per, GR, q, g), q, r1, K);
                         nrows += rp[q] != nullptr;
                     }
                     for (int c = 0; c < nch; ++c) {
                         const int kc0 = c * KC, len = min(KC, K - kc0);
-                        const int sidx = tile % TG_NS;
-                        const uint32_t u = tile / TG_NS;
+                        const int sidx = tile % NS;
+                        const uint32_t u = tile / NS;
                         if (!mbar_wait(&empty[sidx], (u & 1) ^ 1)) P->st->error = ERR_TIMEOUT;
                         const uint32_t bytes = (uint32_t)len * sizeof(T);
                         mbar_expect_tx(&full[sidx], bytes * nrows);
 #pragma unroll
                         for (int q = 0; q < TG_RG; ++q)
-                            if (rp[q]) bulk_g2s(stages + sidx * TG_STAGE + q * TG_ROWB, rp[q] + kc0, bytes, &full[sidx]);
+                            if (rp[q]) bulk_g2s(stages + sidx * stage_bytes + q * rowb, rp[q] + kc0, bytes, &full[sidx]);
                         ++tile;
                     }
                 }
@@ -270,51 +326,67 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
         // ---- stage x for this problem (overlaps the producer's first tiles); every warp
         // must be done with the previous problem's x first
         if (r != lo) named_sync(BAR_C, TG_CONSUMERS);
-        if (EPI == EPI_QKV) c_stage_norm(P->X + (long long)slot * d, w.g1, d, P->eps, xs, cred);
-        else if (EPI == EPI_GATEUP) c_stage_norm(P->X + (long long)slot * d, w.g2, d, P->eps, xs, cred);
+        if (EPI == EPI_QKV) c_stage_norm<T>(P->X + (long long)slot * d, w.g1, d, P->eps, xs, cred);
+        else if (EPI == EPI_GATEUP) c_stage_norm<T>(P->X + (long long)slot * d, w.g2, d, P->eps, xs, cred);
         else if (EPI == EPI_OPROJ) {
-            c_stage_f4(P->ATT + (long long)s * P->q_rows, xs, K);
+            c_stage_f4<T>(P->ATT + (long long)s * P->q_rows, xs, K);
             named_sync(BAR_C, TG_CONSUMERS);
         } else if (EPI == EPI_DOWN) {
-            c_stage_swiglu(P->U + (long long)s * 2 * P->F, xs, K);
+            c_stage_swiglu<T>(P->U + (long long)s * 2 * P->F, xs, K);
             named_sync(BAR_C, TG_CONSUMERS);
         } else {
-            if (s_rows[0] >= 0) c_stage_norm(P->X + (long long)s_rows[0] * d, P->gf, d, P->eps, xs, cred);
+            if (s_rows[0] >= 0) c_stage_norm<T>(P->X + (long long)s_rows[0] * d, P->gf, d, P->eps, xs, cred);
             else {
                 for (int k = tid; k < d; k += TG_CONSUMERS) xs[k] = 0.f;
                 named_sync(BAR_C, TG_CONSUMERS);
             }
-            if (P->Ls > 0) c_stage_norm(P->Xp + (long long)s_rows[1] * d, P->pdm_gf, d, P->eps, xs + d, cred);
+            if (P->Ls > 0) c_stage_norm<T>(P->Xp + (long long)s_rows[1] * d, P->pdm_gf, d, P->eps, xs + d, cred);
             else {
                 for (int k = tid; k < d; k += TG_CONSUMERS) xs[d + k] = 0.f;
                 named_sync(BAR_C, TG_CONSUMERS);
             }
         }
-        for (int g0 = r0; g0 < r1; g0 += GR) {
-            // warp q owns tile row q for all chunks of this group
+        const int per = (r1 - r0 + GR - 1) / GR;
+        for (int g = 0; g < per; ++g) {
+            // warp q owns tile slot q for all chunks of this group
             const int q = warp;
-            const int unit = (GR == TG_RG) ? g0 + q : g0 + (q & 3);
+            const int unit = slot_unit(r0, per, GR, q, g);
             const bool rv = unit < r1;
             float acc0 = 0.f, acc1 = 0.f;
             for (int c = 0; c < nch; ++c) {
                 const int kc0 = c * KC, len = min(KC, K - kc0);
-                const int sidx = tile % TG_NS;
-                const uint32_t u = tile / TG_NS;
+                const int sidx = tile % NS;
+                const uint32_t u = tile / NS;
                 if (!mbar_wait(&full[sidx], u & 1)) P->st->error = ERR_TIMEOUT;
                 if (rv) {
-                    const unsigned char *tb = stages + sidx * TG_STAGE + q * TG_ROWB;
+                    const unsigned char *tb = stages + sidx * stage_bytes + q * rowb;
                     const int nvec = len / VEC;
-                    const float *xk = xs + kc0;
-                    const float *xk1 = (EPI == EPI_LM) ? (TIED ? xs + d + kc0 : (q < 4 ? xs + kc0 : xs + d + kc0)) : xk;
-                    for (int v = lane; v < nvec; v += 32) {
-                        const uint4 wv = *reinterpret_cast<const uint4 *>(tb + v * 16);
+                    // x of this chunk (and of the second right-hand side for the LM head)
+                    const int Kx = EPI == EPI_LM ? d : K, plane = Kx >> 1;
+                    const float *xa = xs + (EPI == EPI_LM && !TIED && q >= 4 ? d : 0);
+                    const float *xb = xs + d;
+                    // vectors lane, lane+32, ... alternate between two accumulator chains
+                    // (fixed order: results do not depend on anything but the row and x)
+                    float c0 = 0.f, c1 = 0.f, e0 = 0.f, e1 = 0.f;
+                    int v = lane;
+                    for (; v + 32 < nvec; v += 64) {
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(tb + v * 16);
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(tb + (v + 32) * 16);
+                        const int f0 = kc0 + v * VEC, f1 = f0 + 32 * VEC;
+                        c0 = dot_x<T>(w0, xa, f0, plane, c0);
+                        c1 = dot_x<T>(w1, xa, f1, plane, c1);
                         if (EPI == EPI_LM && TIED) {
-                            acc0 = dot16(wv, xk + v * VEC, acc0, T());
-                            acc1 = dot16(wv, xk1 + v * VEC, acc1, T());
-                        } else {
-                            acc0 = dot16(wv, xk1 + v * VEC, acc0, T());
+                            e0 = dot_x<T>(w0, xb, f0, plane, e0);
+                            e1 = dot_x<T>(w1, xb, f1, plane, e1);
                         }
                     }
+                    if (v < nvec) {
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(tb + v * 16);
+                        c0 = dot_x<T>(w0, xa, kc0 + v * VEC, plane, c0);
+                        if (EPI == EPI_LM && TIED) e0 = dot_x<T>(w0, xb, kc0 + v * VEC, plane, e0);
+                    }
+                    acc0 += c0 + c1;
+                    if (EPI == EPI_LM && TIED) acc1 += e0 + e1;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[sidx]);
@@ -427,14 +499,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
 }
 
 // ---------------------------------------------------------------------------------
-static int x_bytes(const Plan &h, int epi) {
-    const int K = (epi == EPI_QKV || epi == EPI_GATEUP) ? h.d
-                  : epi == EPI_OPROJ                  ? h.q_rows
-                  : epi == EPI_DOWN                   ? h.F
-                                                      : 2 * h.d;
-    return K * (int)sizeof(float);
-}
-static int smem_for(const Plan &h, int epi) { return TG_NS * TG_STAGE + x_bytes(h, epi); }
+static int smem_for(const Plan &, int) { return TG_SMEM; }
 
 template <typename T, int EPI>
 static void launch_epi(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s) {
