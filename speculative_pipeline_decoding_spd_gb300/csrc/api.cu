@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <cstdlib>
 #include <string>
 #include <vector>
 
@@ -25,12 +26,12 @@ constexpr int SM_BOUND = 256;       // SM count bound used for workspace sizing
 struct spd_handle {
     Plan h{};
     Plan *dP = nullptr;
-    SkPlan sk{};
+    PdmPlan pp{};
     cudaStream_t s_user = nullptr;                 // caller's stream (may be the legacy default stream)
     cudaStream_t s_main = nullptr, s_pdm = nullptr; // own streams: target rounds, draft module
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_in = nullptr, ev_out = nullptr;
     cudaGraphExec_t g1 = nullptr, gN = nullptr;
-    int grid_gemv = 0, grid_lm = 0, num_sms = 0;
+    int grid_gemv = 0, grid_lm = 0, grid_pdm = 0, num_sms = 0;
     bool prefilled = false;
     std::string err;
     float theta = 1e4f;
@@ -109,23 +110,9 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     const int max_chunks = (c->max_seq + ATT_CHUNK - 1) / ATT_CHUNK;
     const int max_steps = n * c->max_new + 2 * n + 8;
     const long long kvs = (long long)c->max_seq * d->Hkv * d->hd;
-    const int NT = (ns + 7) / 8, RP = NT * 8;
-    // draft GEMM partials bound (nks grows with the SM count; SM_BOUND bounds it)
-    const int Ns[5] = {d->d, qkv, d->d, 2 * d->F, d->d};
-    const int Ks[5] = {c->n_anchors * d->d, d->d, qr, d->d, d->F};
-    size_t skp = 1;
-    int max_nrb = 1;
-    for (int i = 0; i < 5; ++i) {
-        const int nrb = (Ns[i] + SK_ROWS - 1) / SK_ROWS;
-        int nks = (2 * SM_BOUND + nrb - 1) / nrb;
-        nks = std::max(1, std::min(nks, Ks[i] / SK_KCHUNK));
-        skp = std::max(skp, (size_t)nks * Ns[i] * RP);
-        max_nrb = std::max(max_nrb, nrb);
-    }
     h.st = b.take<DevState>(1);
     h.X = b.take<float>((size_t)ns * d->d);
     h.QKV = b.take<float>((size_t)n * qkv);
-    h.ATT = b.take<float>((size_t)n * qr);
     h.U = b.take<float>((size_t)n * 2 * d->F);
     h.ANCH = b.take<float>((size_t)ns * c->n_anchors * d->d);
     h.kc = b.take<char>((size_t)d->L * kvs * elem);
@@ -133,17 +120,15 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.pkc = b.take<char>((size_t)std::max(Ls, 1) * kvs * elem);
     h.pvc = b.take<char>((size_t)std::max(Ls, 1) * kvs * elem);
     h.rope = b.take<float2>((size_t)c->max_seq * (d->hd / 2));
-    h.att_part = b.take<float>((size_t)MAXS * d->Hq * max_chunks * (d->hd + 2));
-    h.patt_part = b.take<float>((size_t)MAXS * d->Hq * max_chunks * (d->hd + 2));
+    h.att_part = b.take<float>((size_t)MAXS * d->Hq * max_chunks * (d->hd + 4));
+    h.patt_part = b.take<float>((size_t)MAXS * d->Hq * max_chunks * (d->hd + 4));
     h.att_cnt = b.take<int>((size_t)MAXS * d->Hkv);
     h.patt_cnt = b.take<int>((size_t)MAXS * d->Hkv);
     h.Xp = b.take<float>((size_t)ns * d->d);
     h.QKVp = b.take<float>((size_t)ns * qkv);
     h.ATTp = b.take<float>((size_t)ns * qr);
     h.GUp = b.take<float>((size_t)ns * 2 * d->F);
-    h.inv_rms_p = b.take<float>(MAXS);
-    h.sk_part = b.take<float>(skp);
-    h.sk_cnt = b.take<int>((size_t)max_nrb + 1);
+    h.ssp = b.take<float>((size_t)SM_BOUND * MAXS);
     h.logits = b.take<float>((size_t)2 * d->V);
     h.dlogits = b.take<float>(c->temperature > 0.f ? (size_t)ns * d->V : 1);
     h.lm_part = b.take<float>((size_t)LM_GRID_MAX * 4);
@@ -165,7 +150,6 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.kv_stride = kvs;
     h.att_max_chunks = max_chunks;
     h.max_steps = max_steps;
-    h.sk_max_rowblocks = max_nrb;
     return b.off + 256;
 }
 
@@ -187,7 +171,7 @@ static void record_step(spd_handle *H, std::vector<int> *pairs) {
     Plan *P = H->dP;
     cudaEventRecord(H->ev_fork, H->s_main);
     cudaStreamWaitEvent(H->s_pdm, H->ev_fork, 0);
-    if (h.Ls > 0) launch_pdm_step<T>(P, h, H->sk, H->s_pdm);
+    if (h.Ls > 0) launch_pdm_step<T>(P, h, H->pp, H->grid_pdm, H->s_pdm);
     cudaEventRecord(H->ev_join, H->s_pdm);
     for (int j = 0; j < h.J; ++j) {
         launch_target_qkv<T>(P, h, j, H->grid_gemv, H->s_main);
@@ -260,6 +244,19 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
                 return fail(nullptr, SPD_EINVAL, "null pointer in draft layer " + std::to_string(l));
         }
     }
+    // weight matrices are streamed with 16-byte bulk copies and loads
+    auto a16 = [](const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+    auto layer_ok = [&](const spd_layer_weights &w) {
+        return a16(w.wq) && a16(w.wk) && a16(w.wv) && a16(w.wo) && a16(w.w_gate) && a16(w.w_up) && a16(w.w_down) &&
+               a16(w.attn_norm) && a16(w.ffn_norm);
+    };
+    bool aligned = a16(tw->embed) && a16(tw->lm_head) && a16(tw->final_norm);
+    for (int l = 0; l < d->L; ++l) aligned = aligned && layer_ok(tw->layers[l]);
+    if (Ls > 0) {
+        aligned = aligned && a16(pw->proj) && a16(pw->lm_head) && a16(pw->final_norm);
+        for (int l = 0; l < Ls; ++l) aligned = aligned && layer_ok(pw->layers[l]);
+    }
+    if (!aligned) return fail(nullptr, SPD_EINVAL, "weight pointers must be 16-byte aligned");
     if (c->force_p >= 0.f && (!c->forced_ref || c->forced_ref_len < 1)) return fail(nullptr, SPD_EINVAL, "forced drafts need forced_ref");
     if (!workspace) return fail(nullptr, SPD_EINVAL, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(nullptr, SPD_EINVAL, "workspace must be 256-byte aligned");
@@ -333,13 +330,28 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
         H->err = "no CUDA device";
         return bail(SPD_ECUDA);
     }
-    sk_plan(h, H->num_sms, H->sk);
+    pdm_plan(h, H->pp);
     const int gsm = gemv_smem_bytes(h);
     set_target_attributes(std::max(gsm, 48 * 1024));
-    set_pdm_attributes(std::max(H->sk.smem, 48 * 1024));
+    set_pdm_attributes();
     set_prefill_attributes();
     set_attn_attributes();
+    H->num_sms = std::min(H->num_sms, SM_BOUND);
     H->grid_gemv = H->num_sms * target_blocks_per_sm(h.dtype, gemv_smem_bytes(h));
+    // The draft module's GEMMs run on their own stream.  With pdm_sms > 0 they use that many
+    // CTAs (one per SM) and the target's GEMVs the remaining SMs, so both streams stream
+    // weights side by side; with 0 each launch spans the whole GPU and the two take turns.
+    H->grid_pdm = H->num_sms;
+    if (Ls > 0) {
+        int pdm_sms = -1;
+        if (const char *e = std::getenv("SPD_PDM_SMS")) pdm_sms = std::atoi(e);
+        if (pdm_sms < 0) pdm_sms = 0;
+        if (pdm_sms > 0 && pdm_sms < H->num_sms) {
+            H->grid_pdm = pdm_sms;
+            H->grid_gemv = H->num_sms - pdm_sms;
+        }
+    }
+    h.pdm_grid = H->grid_pdm;
     H->grid_lm = std::min(LM_GRID_MAX, H->num_sms * lm_blocks_per_sm(h.dtype, 2 * h.d * 4, h.pdm_lm_head == h.lm_head));
     if (cudaStreamCreateWithFlags(&H->s_main, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&H->s_pdm, cudaStreamNonBlocking) != cudaSuccess ||
@@ -361,7 +373,6 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
     if (cudaMemsetAsync(workspace, 0, (char *)h.kc - (char *)workspace, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.att_cnt, 0, sizeof(int) * MAXS * h.Hkv, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.patt_cnt, 0, sizeof(int) * MAXS * h.Hkv, H->s_main) != cudaSuccess ||
-        cudaMemsetAsync(h.sk_cnt, 0, sizeof(int) * (h.sk_max_rowblocks + 1), H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.lm_cnt, 0, sizeof(int), H->s_main) != cudaSuccess) {
         H->err = "workspace initialisation failed";
         return bail(SPD_ECUDA);

@@ -1,23 +1,37 @@
 // Decode attention device code shared by the pipeline step (k_attn.cu) and the
 // standalone attention entry points (k_ops.cu).
 //
-// Split-K over fixed 128-position chunks: one CTA per (problem, kv head, chunk) holds
-// the whole GQA group.  The chunk's K and V rows are staged in shared memory with all
-// 16-byte loads in flight, scores are computed one position per thread, the weighted
-// sum one (dim pair, position group) per thread.  The last CTA of a (problem, kv head)
-// merges the chunks in chunk order.  Chunk boundaries depend only on the position, so
-// results do not depend on what else shares a launch.
+// Split-K over fixed 128-position chunks: one CTA of 256 threads per (problem, kv head,
+// chunk) holds the whole GQA group.  Latency is what bounds this kernel (a decode step
+// reads a few MB of K/V spread over hundreds of CTAs), so every global access is issued
+// as early as possible and all of a thread's loads are in flight together:
+//   * the chunk's K and V rows go to shared memory by asynchronous 16-byte copies (no
+//     registers held while they are in flight), q is staged (and rotated) meanwhile;
+//   * scores: thread = (position, head parity), 16-byte K reads from a row pitch that
+//     puts 8 consecutive rows on distinct banks, q broadcast from shared memory;
+//   * softmax per head in one warp, then o = sum_j p_j v_j with thread = (16-byte vector
+//     of the row, position group), 4 heads per pass; position groups are added by a fixed
+//     shuffle tree inside a warp, the warps in warp order through shared memory;
+//   * the chunk's (o, max, sum) go to the partial buffer; the last CTA of a (problem, kv
+//     head) merges the chunks in chunk order with all loads in flight (or, without
+//     arrival counters, the consumer of the output merges them).
+// Chunk boundaries depend only on the position and each reduction has a fixed order, so
+// the result does not depend on what else shares a launch.
 #pragma once
 
 #include "common.cuh"
 
 namespace spd {
 
-constexpr int ATT_THREADS = 128;
+constexpr int ATT_THREADS = 256;
 constexpr int ATT_MAXG = 8;     // query heads per kv head
 constexpr int ATT_MAXHD = 128;
+constexpr int ATT_HB = 4;       // heads per weighted-sum pass
+// CTAs per SM the register budget is sized for: one wave for 8 stages x 8 kv heads of a
+// 2K-position context
+template <typename T> __host__ __device__ constexpr int att_min_blocks() { return sizeof(T) == 2 ? 3 : 1; }
 
-// K/V tiles live in shared memory as 32-bit words: bf16 pairs (T = bf16) or floats.
+// K and V rows live in shared memory as 32-bit words: bf16 pairs (T = bf16) or floats.
 template <typename T> struct KVW {
     static constexpr int PER = 2;   // elements per word
     __device__ static __forceinline__ uint32_t pack(float a, float b) {
@@ -31,12 +45,17 @@ template <> struct KVW<float> {
 
 template <typename T>
 __host__ __device__ constexpr int att_words(int hd) { return hd / KVW<T>::PER; }
-
-// dynamic shared memory: Ks [CHUNK][words+1] (odd pitch: one-row-per-thread reads hit
-// distinct banks), Vs [CHUNK][words]
+// row pitch in words: 16 bytes more than the row, so the 16-byte reads of 8 consecutive
+// rows at one column fall on 8 distinct 16-byte bank groups
 template <typename T>
-__host__ __device__ constexpr int att_smem_bytes(int hd) {
-    return (ATT_CHUNK * (att_words<T>(hd) + 1) + ATT_CHUNK * att_words<T>(hd)) * 4;
+__host__ __device__ constexpr int att_pitch(int hd) { return att_words<T>(hd) + 4; }
+
+// dynamic shared memory (bytes): Ks [CHUNK][pitch] | Vs [CHUNK][pitch] words, then
+// qs [G][hd] and the scores [G][CHUNK] as floats.  After the scores the K rows hold the
+// per-warp weighted sums [8 warps][ATT_HB][hd] floats (16 KB at hd 128, below the K rows).
+template <typename T>
+__host__ __device__ constexpr int att_smem_bytes(int hd, int G) {
+    return 2 * ATT_CHUNK * att_pitch<T>(hd) * 4 + G * hd * 4 + G * ATT_CHUNK * 4;
 }
 
 // One attention problem: a single query token of Hq heads against cache positions
@@ -51,8 +70,9 @@ struct AttnArgs {
     T *vc;
     int S;                   // attended positions 0..S-1
     float *out;              // [Hq][hd]
-    float *part;             // split-K partials [prob][Hq][maxch][hd+2]
-    int *cnt;                // [prob][Hkv] arrival counters (zero between launches)
+    float *part;             // split-K partials [prob][Hq][maxch][att_part_pitch(hd)]
+    int *cnt;                // [prob][Hkv] arrival counters (zero between launches), or nullptr:
+                             // no merge here, every chunk (even a single one) leaves its partial
     int prob, maxch, Hq, Hkv, hd;
     float scale;
 };
@@ -62,74 +82,54 @@ struct AttnArgs {
 template <typename T>
 __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
     extern __shared__ __align__(16) uint32_t kv_smem[];
-    __shared__ __align__(16) float qs[ATT_MAXG][ATT_MAXHD];
-    __shared__ float sc[ATT_MAXG][ATT_CHUNK];
     __shared__ float knew[ATT_MAXHD], vnew[ATT_MAXHD];
     __shared__ float s_m[ATT_MAXG], s_l[ATT_MAXG];
-    __shared__ float ored[4][ATT_MAXG][ATT_MAXHD];
     __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hd = a.hd, Hkv = a.Hkv, G = a.Hq / Hkv, half = hd / 2;
     const int S = a.S, pos = S - 1, nch = (S + ATT_CHUNK - 1) / ATT_CHUNK;
     const int j0 = c * ATT_CHUNK, cnt = min(ATT_CHUNK, S - j0);
     const long long rowstride = (long long)Hkv * hd;
     const bool owner = a.kraw != nullptr && (c == nch - 1);
-    const int W = att_words<T>(hd), KP = W + 1;
+    const int W = att_words<T>(hd), KP = att_pitch<T>(hd);
     uint32_t *Ks = kv_smem, *Vs = kv_smem + ATT_CHUNK * KP;
+    float *qs = reinterpret_cast<float *>(Vs + ATT_CHUNK * KP);   // [G][hd]
+    float *sc = qs + G * hd;                                       // [G][CHUNK]
 
-    // ---- stage this chunk's K and V rows of kv head g (2 x 8 16-byte loads in flight)
+    // ---- this chunk's K and V rows of kv head g: asynchronous 16-byte copies
     {
-        const int vec_per_row = hd * (int)sizeof(T) / 16;
-        const int total = cnt * vec_per_row;
-        constexpr int U = 8;
-        for (int b = threadIdx.x; b < total; b += U * blockDim.x) {
-            uint4 kv[U], vv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int idx = b + u * blockDim.x;
-                if (idx < total) {
-                    const int j = idx / vec_per_row, q = idx - j * vec_per_row;
-                    const long long off = (long long)(j0 + j) * rowstride + (long long)g * hd;
-                    kv[u] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(a.kc + off) + 16 * q);
-                    vv[u] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(a.vc + off) + 16 * q);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int idx = b + u * blockDim.x;
-                if (idx < total) {
-                    const int j = idx / vec_per_row, q = idx - j * vec_per_row;
-                    uint32_t *kd = Ks + j * KP + 4 * q;
-                    kd[0] = kv[u].x;
-                    kd[1] = kv[u].y;
-                    kd[2] = kv[u].z;
-                    kd[3] = kv[u].w;
-                    *reinterpret_cast<uint4 *>(Vs + j * W + 4 * q) = vv[u];
-                }
-            }
+        const int vpr = hd * (int)sizeof(T) / 16;   // 16-byte vectors per row
+        const int total = cnt * vpr;
+        const long long base = ((long long)j0 * rowstride + (long long)g * hd) * (long long)sizeof(T);
+        const char *kb = reinterpret_cast<const char *>(a.kc) + base;
+        const char *vb = reinterpret_cast<const char *>(a.vc) + base;
+        for (int idx = tid; idx < total; idx += ATT_THREADS) {
+            const int j = idx / vpr, q = idx - j * vpr;
+            const long long off = (long long)j * rowstride * (long long)sizeof(T) + 16 * q;
+            cp_async16(Ks + j * KP + 4 * q, kb + off);
+            cp_async16(Vs + j * KP + 4 * q, vb + off);
         }
     }
     // ---- q (rotated here when raw), k_new / v_new appended by the chunk owner
     if (a.rope) {
-        for (int idx = threadIdx.x; idx < G * half; idx += blockDim.x) {
-            const int h = idx / half, i = idx % half;
+        for (int idx = tid; idx < G * half; idx += ATT_THREADS) {
+            const int h = idx / half, i = idx - h * half;
             const float *qh = a.q + (long long)(g * G + h) * hd;
             const float2 r = a.rope[i];
             const float x0 = qh[i], x1 = qh[i + half];
-            qs[h][i] = x0 * r.x - x1 * r.y;
-            qs[h][i + half] = x1 * r.x + x0 * r.y;
+            qs[h * hd + i] = x0 * r.x - x1 * r.y;
+            qs[h * hd + i + half] = x1 * r.x + x0 * r.y;
         }
     } else {
-        for (int idx = threadIdx.x; idx < G * hd; idx += blockDim.x) {
-            const int h = idx / hd, i = idx % hd;
-            qs[h][i] = a.q[(long long)(g * G + h) * hd + i];
-        }
+        for (int idx = tid; idx < G * hd; idx += ATT_THREADS) qs[idx] = a.q[(long long)g * G * hd + idx];
     }
     if (owner) {
         const float *kh = a.kraw + (long long)g * hd;
         const float *vh = a.vraw + (long long)g * hd;
         T *kdst = a.kc + (long long)pos * rowstride + (long long)g * hd;
         T *vdst = a.vc + (long long)pos * rowstride + (long long)g * hd;
-        for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        if (tid < half) {
+            const int i = tid;
             const float2 r = a.rope[i];
             const float x0 = kh[i], x1 = kh[i + half];
             const auto k0 = WTraits<T>::store(x0 * r.x - x1 * r.y);
@@ -138,67 +138,84 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
             kdst[i + half] = k1;
             knew[i] = (float)k0;
             knew[i + half] = (float)k1;
-        }
-        for (int i = threadIdx.x; i < hd; i += blockDim.x) {
+        } else if (tid < half + hd) {
+            const int i = tid - half;
             const auto v0 = WTraits<T>::store(vh[i]);
             vdst[i] = v0;
             vnew[i] = (float)v0;
         }
     }
+    cp_async_wait_all();
     __syncthreads();
     if (owner) {
         // the new position's row comes from this kernel's own (rounded) values
         const int j = pos - j0;
-        for (int w = threadIdx.x; w < W; w += blockDim.x) {
+        for (int w = tid; w < W; w += ATT_THREADS) {
             if constexpr (KVW<T>::PER == 2) {
                 Ks[j * KP + w] = KVW<T>::pack(knew[2 * w], knew[2 * w + 1]);
-                Vs[j * W + w] = KVW<T>::pack(vnew[2 * w], vnew[2 * w + 1]);
+                Vs[j * KP + w] = KVW<T>::pack(vnew[2 * w], vnew[2 * w + 1]);
             } else {
                 Ks[j * KP + w] = __float_as_uint(knew[w]);
-                Vs[j * W + w] = __float_as_uint(vnew[w]);
+                Vs[j * KP + w] = __float_as_uint(vnew[w]);
             }
         }
         __syncthreads();
     }
 
-    // ---- scores: thread = position, all heads of the group
+    // ---- scores: thread = (position j, head parity hh); heads hh, hh + 2, ...
     {
-        const int j = threadIdx.x;
-        float acc[ATT_MAXG];
+        const int j = tid & (ATT_CHUNK - 1), hh = tid / ATT_CHUNK;
+        float acc[ATT_MAXG / 2];
 #pragma unroll
-        for (int h = 0; h < ATT_MAXG; ++h) acc[h] = 0.f;
-        if (j < cnt) {
+        for (int u = 0; u < ATT_MAXG / 2; ++u) acc[u] = 0.f;
+        if (j < cnt && hh < G) {
             const uint32_t *kr = Ks + j * KP;
-            for (int w = 0; w < W; ++w) {
-                const uint32_t u = kr[w];
+            for (int w = 0; w < W; w += 4) {
+                const uint4 kw = *reinterpret_cast<const uint4 *>(kr + w);
+                float k[8];
+                int e0;   // element index of kw.x
                 if constexpr (KVW<T>::PER == 2) {
-                    const float k0 = bf_lo(u), k1 = bf_hi(u);
-#pragma unroll
-                    for (int h = 0; h < ATT_MAXG; ++h)
-                        if (h < G) acc[h] = fmaf(qs[h][2 * w + 1], k1, fmaf(qs[h][2 * w], k0, acc[h]));
+                    k[0] = bf_lo(kw.x); k[1] = bf_hi(kw.x); k[2] = bf_lo(kw.y); k[3] = bf_hi(kw.y);
+                    k[4] = bf_lo(kw.z); k[5] = bf_hi(kw.z); k[6] = bf_lo(kw.w); k[7] = bf_hi(kw.w);
+                    e0 = 2 * w;
                 } else {
-                    const float k0 = __uint_as_float(u);
+                    k[0] = __uint_as_float(kw.x); k[1] = __uint_as_float(kw.y);
+                    k[2] = __uint_as_float(kw.z); k[3] = __uint_as_float(kw.w);
+                    e0 = w;
+                }
 #pragma unroll
-                    for (int h = 0; h < ATT_MAXG; ++h)
-                        if (h < G) acc[h] = fmaf(qs[h][w], k0, acc[h]);
+                for (int u = 0; u < ATT_MAXG / 2; ++u) {
+                    const int h = hh + 2 * u;
+                    if (h < G) {
+                        const float4 q0 = *reinterpret_cast<const float4 *>(qs + h * hd + e0);
+                        float s = acc[u];
+                        s = fmaf(q0.x, k[0], s); s = fmaf(q0.y, k[1], s); s = fmaf(q0.z, k[2], s); s = fmaf(q0.w, k[3], s);
+                        if constexpr (KVW<T>::PER == 2) {
+                            const float4 q1 = *reinterpret_cast<const float4 *>(qs + h * hd + e0 + 4);
+                            s = fmaf(q1.x, k[4], s); s = fmaf(q1.y, k[5], s); s = fmaf(q1.z, k[6], s); s = fmaf(q1.w, k[7], s);
+                        }
+                        acc[u] = s;
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int h = 0; h < ATT_MAXG; ++h)
-            if (h < G) sc[h][j] = j < cnt ? acc[h] * a.scale : -INFINITY;
+        for (int u = 0; u < ATT_MAXG / 2; ++u) {
+            const int h = hh + 2 * u;
+            if (h < G) sc[h * ATT_CHUNK + j] = j < cnt ? acc[u] * a.scale : -INFINITY;
+        }
     }
     __syncthreads();
     // ---- chunk softmax per head
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int h = warp; h < G; h += ATT_THREADS / 32) {
+        float *sh = sc + h * ATT_CHUNK;
         float m = -INFINITY;
-        for (int j = lane; j < cnt; j += 32) m = fmaxf(m, sc[h][j]);
+        for (int j = lane; j < cnt; j += 32) m = fmaxf(m, sh[j]);
         m = warp_max(m);
         float l = 0.f;
         for (int j = lane; j < ATT_CHUNK; j += 32) {
-            const float e = j < cnt ? expf(sc[h][j] - m) : 0.f;
-            sc[h][j] = e;
+            const float e = j < cnt ? expf(sh[j] - m) : 0.f;
+            sh[j] = e;
             l += e;
         }
         l = warp_sum(l);
@@ -208,81 +225,105 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
         }
     }
     __syncthreads();
-    // ---- o = sum_j p_j v_j : thread = (dim pair, position group); shared-memory reads only
-    const int npair = hd / 2;
-    const int nq = ATT_THREADS / npair;       // 2 (hd 128) or 4 (hd 64) position groups
-    const int dp = threadIdx.x % npair, qg = threadIdx.x / npair;
-    float o0[ATT_MAXG], o1[ATT_MAXG];
-#pragma unroll
-    for (int h = 0; h < ATT_MAXG; ++h) o0[h] = o1[h] = 0.f;
-    for (int j = qg; j < cnt; j += nq) {
-        float v0, v1;
-        if constexpr (KVW<T>::PER == 2) {
-            const uint32_t u = Vs[j * W + dp];
-            v0 = bf_lo(u);
-            v1 = bf_hi(u);
-        } else {
-            v0 = __uint_as_float(Vs[j * W + 2 * dp]);
-            v1 = __uint_as_float(Vs[j * W + 2 * dp + 1]);
-        }
-#pragma unroll
-        for (int h = 0; h < ATT_MAXG; ++h)
-            if (h < G) {
-                const float p = sc[h][j];
-                o0[h] = fmaf(p, v0, o0[h]);
-                o1[h] = fmaf(p, v1, o1[h]);
-            }
-    }
-#pragma unroll
-    for (int h = 0; h < ATT_MAXG; ++h)
-        if (h < G) {
-            ored[qg][h][2 * dp] = o0[h];
-            ored[qg][h][2 * dp + 1] = o1[h];
-        }
-    __syncthreads();
+    // ---- o = sum_j p_j v_j: thread = (16-byte vector vo of the row, position group qg),
+    // positions qg, qg + NQ, ...; ATT_HB heads per pass
     auto pidx = [&](int h, int cc) -> long long {
-        return (((long long)a.prob * a.Hq + g * G + h) * a.maxch + cc) * (hd + 2);
+        return (((long long)a.prob * a.Hq + g * G + h) * a.maxch + cc) * att_part_pitch(hd);
     };
-    for (int idx = threadIdx.x; idx < G * hd; idx += blockDim.x) {
-        const int h = idx / hd, dd = idx % hd;
-        float o = ored[0][h][dd];
-        for (int q = 1; q < nq; ++q) o += ored[q][h][dd];
-        if (nch == 1) {
-            a.out[(long long)(g * G + h) * hd + dd] = o / s_l[h];
-        } else {
-            a.part[pidx(h, c) + dd] = o;
-            if (dd == 0) {
-                a.part[pidx(h, c) + hd] = s_m[h];
-                a.part[pidx(h, c) + hd + 1] = s_l[h];
+    constexpr int EPV = 16 / (int)sizeof(T);        // elements per vector
+    const int LPR = hd / EPV, NQ = ATT_THREADS / LPR;
+    const int vo = tid % LPR, qg = tid / LPR;
+    float *ored = reinterpret_cast<float *>(kv_smem);   // [8 warps][ATT_HB][hd], over the K rows
+    for (int hb = 0; hb < G; hb += ATT_HB) {
+        float o[ATT_HB][EPV];
+#pragma unroll
+        for (int u = 0; u < ATT_HB; ++u)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) o[u][e] = 0.f;
+        for (int j = qg; j < cnt; j += NQ) {
+            const uint4 vw = *reinterpret_cast<const uint4 *>(Vs + j * KP + 4 * vo);
+            float v[EPV];
+            if constexpr (sizeof(T) == 2) {
+                v[0] = bf_lo(vw.x); v[1] = bf_hi(vw.x); v[2] = bf_lo(vw.y); v[3] = bf_hi(vw.y);
+                v[4] = bf_lo(vw.z); v[5] = bf_hi(vw.z); v[6] = bf_lo(vw.w); v[7] = bf_hi(vw.w);
+            } else {
+                v[0] = __uint_as_float(vw.x); v[1] = __uint_as_float(vw.y);
+                v[2] = __uint_as_float(vw.z); v[3] = __uint_as_float(vw.w);
+            }
+#pragma unroll
+            for (int u = 0; u < ATT_HB; ++u)
+                if (hb + u < G) {
+                    const float p = sc[(hb + u) * ATT_CHUNK + j];
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) o[u][e] = fmaf(p, v[e], o[u][e]);
+                }
+        }
+        for (int off = LPR; off < 32; off <<= 1)
+#pragma unroll
+            for (int u = 0; u < ATT_HB; ++u)
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) o[u][e] += __shfl_xor_sync(0xffffffffu, o[u][e], off);
+        if (hb > 0) __syncthreads();   // the previous pass's sums have been read
+        if (lane < LPR) {
+#pragma unroll
+            for (int u = 0; u < ATT_HB; ++u)
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) ored[(warp * ATT_HB + u) * hd + vo * EPV + e] = o[u][e];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < ATT_HB * hd; idx += ATT_THREADS) {
+            const int u = idx / hd, dd = idx - u * hd, h = hb + u;
+            if (h >= G) continue;
+            float oo = ored[u * hd + dd];
+            for (int w = 1; w < ATT_THREADS / 32; ++w) oo += ored[(w * ATT_HB + u) * hd + dd];
+            if (nch == 1 && a.cnt) {
+                a.out[(long long)(g * G + h) * hd + dd] = oo / s_l[h];
+            } else {
+                a.part[pidx(h, c) + dd] = oo;
+                if (dd == 0) {
+                    a.part[pidx(h, c) + hd] = s_m[h];
+                    a.part[pidx(h, c) + hd + 1] = s_l[h];
+                }
             }
         }
     }
-    if (nch == 1) return;
+    if (nch == 1 || !a.cnt) return;
     int *cntp = a.cnt + a.prob * Hkv + g;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(cntp, 1) == nch - 1;
+    if (tid == 0) s_last = atomicAdd(cntp, 1) == nch - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // ---- merge in chunk order: weights e^{m_c - M} per (head, chunk) staged first, then each
-    // thread combines its (head, dim) outputs with 8 chunk loads in flight before the adds
-    float *mw = &sc[0][0];   // reuse: [G][ATT_CHUNK] chunk weights (nch <= ATT_CHUNK)
+    // ---- merge in chunk order.  Chunk weights e^{m_c - M}: one warp per head, one lane per
+    // chunk (32 at a time, loads in flight together), denominators by a fixed shuffle tree
+    // per 32-chunk block added in block order
+    float *mw = sc;   // [G][ATT_CHUNK] chunk weights (nch <= ATT_CHUNK)
     for (int h = warp; h < G; h += ATT_THREADS / 32) {
+        float mv[ATT_CHUNK / 32], lv[ATT_CHUNK / 32];
         float M = -INFINITY;
-        for (int cc = lane; cc < nch; cc += 32) M = fmaxf(M, __ldcg(a.part + pidx(h, cc) + hd));
+#pragma unroll
+        for (int b = 0; b < ATT_CHUNK / 32; ++b) {
+            const int cc = b * 32 + lane;
+            mv[b] = cc < nch ? __ldcg(a.part + pidx(h, cc) + hd) : -INFINITY;
+            lv[b] = cc < nch ? __ldcg(a.part + pidx(h, cc) + hd + 1) : 0.f;
+        }
+#pragma unroll
+        for (int b = 0; b < ATT_CHUNK / 32; ++b) M = fmaxf(M, mv[b]);
         M = warp_max(M);
         float den = 0.f;
-        for (int cc = 0; cc < nch; ++cc) {
-            const float w = expf(__ldcg(a.part + pidx(h, cc) + hd) - M);
-            if (lane == 0) mw[h * ATT_CHUNK + cc] = w;
-            den = fmaf(w, __ldcg(a.part + pidx(h, cc) + hd + 1), den);
+#pragma unroll
+        for (int b = 0; b < ATT_CHUNK / 32; ++b) {
+            const int cc = b * 32 + lane;
+            const float w = cc < nch ? expf(mv[b] - M) : 0.f;
+            if (cc < nch) mw[h * ATT_CHUNK + cc] = w;
+            den += warp_sum(w * lv[b]);
         }
         if (lane == 0) s_l[h] = den;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G * hd; idx += blockDim.x) {
-        const int h = idx / hd, dd = idx % hd;
+    for (int idx = tid; idx < G * hd; idx += ATT_THREADS) {
+        const int h = idx / hd, dd = idx - h * hd;
         float vals[8];
         float num = 0.f;
         for (int c0 = 0; c0 < nch; c0 += 8) {
@@ -294,7 +335,7 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
         }
         a.out[(long long)(g * G + h) * hd + dd] = num / s_l[h];
     }
-    if (threadIdx.x == 0) *cntp = 0;
+    if (tid == 0) *cntp = 0;
 }
 
 }  // namespace spd

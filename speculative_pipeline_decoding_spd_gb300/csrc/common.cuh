@@ -7,7 +7,7 @@
 //   X   fp32 [n+1][d]            residual stream per slot
 //   ANCH fp32 [n+1][nB][d]       anchor states per slot (depth a = after a layers, 0 = embedding)
 //   QKV fp32 [n][(Hq+2Hkv) hd]   raw q,k,v of each stage (RoPE is applied by the attention kernel)
-//   ATT fp32 [n][Hq hd]          attention output of each stage
+//   att_part fp32 [stage][Hq][chunk][hd+4]  attention chunk partials (merged by the O projection)
 //   U   fp32 [n][2F]             raw gate and up sums of each stage (SiLU(gate)*up formed by the down GEMV)
 //   K/V cache per target layer   dtype [max_seq][Hkv][hd]; valid length per layer in DevState
 //   draft module buffers         Xp [n+1][d], QKVp/ATTp/GUp per row, its own K/V cache
@@ -27,10 +27,10 @@ constexpr int MAXL = SPD_MAX_LAYERS;
 constexpr int MAXPL = SPD_MAX_PDM_LAYERS;
 constexpr int MAXB = SPD_MAX_ANCHORS;
 constexpr int ATT_CHUNK = 128;           // positions per attention split (fixed: results independent of grouping)
+// floats per attention partial row (one head, one chunk): o[hd], max, sum, 2 pad (16-byte rows)
+__host__ __device__ constexpr int att_part_pitch(int hd) { return hd + 4; }
 constexpr int GEMV_THREADS = 256;
 constexpr int GEMV_WARPS = GEMV_THREADS / 32;
-constexpr int SK_ROWS = 128;             // rows per CTA of the draft-module skinny GEMM (8 warps x 16)
-constexpr int SK_KCHUNK = 64;            // K elements per mma iteration (two m16n8k16 steps)
 constexpr int MAX_R = MAXS;              // draft-module rows per step (n+1)
 
 // device error codes (DevState::error)
@@ -79,20 +79,19 @@ struct Plan {
     LayerW tl[MAXL];
     LayerW pl[MAXPL];
     // workspace
-    float *X, *QKV, *ATT, *U, *ANCH;   // U: [n][2F] gate | up
+    float *X, *QKV, *U, *ANCH;   // U: [n][2F] gate | up
     void *kc, *vc, *pkc, *pvc;
     long long kv_stride;           // elements per layer cache
     float2 *rope;                  // [max_seq][hd/2] (cos, sin)
-    float *att_part, *patt_part;   // [MAXS][Hq][max_chunks][hd + 2] (target / draft module)
+    float *att_part, *patt_part;   // [MAXS][Hq][max_chunks][hd + 4] (target per stage / draft module per row)
     int *att_cnt, *patt_cnt;       // [MAXS][Hkv]
     int att_max_chunks;
     long long layer_bytes;         // weight bytes of one target layer
     long long pdm_bytes;           // draft module per step (projection + layers)
     long long lm_bytes;            // LM head per step
-    float *Xp, *QKVp, *ATTp, *GUp, *inv_rms_p;
-    float *sk_part;                // draft skinny GEMM split-K partials
-    int *sk_cnt;                   // per row-block counters + 1 global
-    int sk_max_rowblocks, sk_max_kseg;
+    float *Xp, *QKVp, *ATTp, *GUp;  // draft module rows: residual, q|k|v, attention, gate|up
+    float *ssp;                    // [pdm_grid][MAXS] per-CTA sums of squares of the Xp rows
+    int pdm_grid;                  // CTAs of every draft GEMM launch
     float *logits;                 // [2][V]
     float *dlogits;                // [n+1][V] draft logits per slot (T > 0)
     float *lm_part;                // [grid][2] (val, idx as float bits)
@@ -149,6 +148,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
+// Asynchronous 16-byte global -> shared copy (no register staging); wait_all waits for all
+// of the thread's outstanding copies.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Barrier among the first `threads` threads of the CTA (id 0 is __syncthreads').
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -427,15 +432,16 @@ template <typename T> void launch_target_oproj(const Plan *P, const Plan &h, int
 template <typename T> void launch_target_gateup(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
 template <typename T> void launch_target_down(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
 template <typename T> void launch_lm_head(const Plan *P, const Plan &h, int grid, cudaStream_t s);
-struct SkPlan { int nks[5]; int smem; int NT; };   // split-K per draft GEMM: proj, qkv, o, gateup, down
-template <typename T> void launch_pdm_step(const Plan *P, const Plan &h, const SkPlan &sk, cudaStream_t s);
+// draft GEMMs (proj, qkv, o, gate/up, down): K slab width and slab count; MT = 16-row mma tiles of x
+struct PdmPlan { int kx[5]; int ns[5]; int MT; };
+template <typename T> void launch_pdm_step(const Plan *P, const Plan &h, const PdmPlan &pp, int grid, cudaStream_t s);
 template <typename T> void launch_pdm_attn(const Plan *P, const Plan &h, int layer, cudaStream_t s);
-void sk_plan(const Plan &h, int num_sms, SkPlan &sk);
-void set_pdm_attributes(int smem);
+void pdm_plan(const Plan &h, PdmPlan &pp);
+void set_pdm_attributes();
 void set_target_attributes(int smem);
 void set_prefill_attributes();
 void set_attn_attributes();
-int attn_smem_bytes(int dtype, int hd);
+int attn_smem_bytes(int dtype, int hd, int G);
 template <typename T> void launch_verify(const Plan *P, const Plan &h, cudaStream_t s);
 template <typename T> void launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int grid,
                                           cudaStream_t s);

@@ -17,7 +17,7 @@ namespace spd {
 // Plan-driven launch: problems are the occupied stages with a layer at this round
 // (TARGET) or the draft module's rows (draft layer `arg`).
 template <typename T, bool TARGET>
-__global__ void __launch_bounds__(ATT_THREADS) k_attn(const Plan *__restrict__ P, int arg) {
+__global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const Plan *__restrict__ P, int arg) {
     __shared__ int s_ok, s_pos, s_layer, s_src;
     const int Hkv = P->Hkv, hd = P->hd;
     const int g = blockIdx.x % Hkv, c = blockIdx.x / Hkv, prob = blockIdx.y;
@@ -68,9 +68,10 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const Plan *__restrict__ P
         a.rope = P->rope + (long long)s_pos * (hd / 2);
         a.kraw = raw + P->q_rows;
         a.vraw = raw + P->q_rows + P->kv_rows;
-        a.out = P->ATT + (long long)s_src * P->q_rows;
+        a.out = nullptr;
         a.part = P->att_part;
-        a.cnt = P->att_cnt;
+        a.cnt = nullptr;   // the O projection merges the chunks while staging its input
+        a.prob = s_src;    // partials indexed by stage
     } else {
         a.q = P->QKVp + (long long)s_src * P->qkv_rows;
         a.rope = nullptr;
@@ -83,28 +84,36 @@ __global__ void __launch_bounds__(ATT_THREADS) k_attn(const Plan *__restrict__ P
     attn_cta<T>(a, g, c);
 }
 
-int attn_smem_bytes(int dtype, int hd) {
-    return dtype == SPD_BF16 ? att_smem_bytes<__nv_bfloat16>(hd) : att_smem_bytes<float>(hd);
+int attn_smem_bytes(int dtype, int hd, int G) {
+    return dtype == SPD_BF16 ? att_smem_bytes<__nv_bfloat16>(hd, G) : att_smem_bytes<float>(hd, G);
 }
 
 void set_attn_attributes() {
-    cudaFuncSetAttribute(k_attn<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem_bytes<float>(128));
-    cudaFuncSetAttribute(k_attn<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, att_smem_bytes<float>(128));
+    cudaFuncSetAttribute(k_attn<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         att_smem_bytes<float>(ATT_MAXHD, ATT_MAXG));
+    cudaFuncSetAttribute(k_attn<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         att_smem_bytes<float>(ATT_MAXHD, ATT_MAXG));
     cudaFuncSetAttribute(k_attn<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         att_smem_bytes<__nv_bfloat16>(128));
+                         att_smem_bytes<__nv_bfloat16>(ATT_MAXHD, ATT_MAXG));
     cudaFuncSetAttribute(k_attn<__nv_bfloat16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         att_smem_bytes<__nv_bfloat16>(128));
+                         att_smem_bytes<__nv_bfloat16>(ATT_MAXHD, ATT_MAXG));
+    cudaFuncSetAttribute(k_attn<float, true>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(k_attn<float, false>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(k_attn<__nv_bfloat16, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(k_attn<__nv_bfloat16, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
 }
 
 template <typename T>
 void launch_target_attn(const Plan *P, const Plan &h, int round, cudaStream_t s) {
     dim3 grid(h.att_max_chunks * h.Hkv, h.n);
-    k_attn<T, true><<<grid, ATT_THREADS, att_smem_bytes<T>(h.hd), s>>>(P, round);
+    k_attn<T, true><<<grid, ATT_THREADS, att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s>>>(P, round);
 }
 template <typename T>
 void launch_pdm_attn(const Plan *P, const Plan &h, int layer, cudaStream_t s) {
     dim3 grid(h.att_max_chunks * h.Hkv, h.n + 1);
-    k_attn<T, false><<<grid, ATT_THREADS, att_smem_bytes<T>(h.hd), s>>>(P, layer);
+    k_attn<T, false><<<grid, ATT_THREADS, att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s>>>(P, layer);
 }
 
 template void launch_target_attn<float>(const Plan *, const Plan &, int, cudaStream_t);

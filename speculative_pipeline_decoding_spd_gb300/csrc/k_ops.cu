@@ -21,10 +21,10 @@ int ops_fail(int code, const std::string &msg) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Bytes of split-K scratch one call needs: Hkv counters (256-byte padded), then the
-// [Hq][chunks][hd + 2] partials.
+// [Hq][chunks][hd + 4] partials.
 size_t attn_scratch_bytes(int Hq, int Hkv, int hd, int seq_len) {
     const int nch = (seq_len + ATT_CHUNK - 1) / ATT_CHUNK;
-    return align256((size_t)Hkv * sizeof(int)) + (size_t)Hq * nch * (hd + 2) * sizeof(float);
+    return align256((size_t)Hkv * sizeof(int)) + (size_t)Hq * nch * att_part_pitch(hd) * sizeof(float);
 }
 
 int attn_validate(int dtype, int Hq, int Hkv, int hd, int seq_len, const void *q, const void *k, const void *v,
@@ -43,7 +43,7 @@ int attn_validate(int dtype, int Hq, int Hkv, int hd, int seq_len, const void *q
 }
 
 template <typename T>
-__global__ void __launch_bounds__(ATT_THREADS) k_attn_direct(AttnArgs<T> a) {
+__global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn_direct(AttnArgs<T> a) {
     attn_cta<T>(a, blockIdx.x % a.Hkv, blockIdx.x / a.Hkv);
 }
 
@@ -62,14 +62,14 @@ int attn_launch(int dtype, int Hq, int Hkv, int hd, int seq_len, const float *q,
                                   const_cast<__nv_bfloat16 *>(reinterpret_cast<const __nv_bfloat16 *>(k)),
                                   const_cast<__nv_bfloat16 *>(reinterpret_cast<const __nv_bfloat16 *>(v)), seq_len,
                                   out, part, cnt, 0, nch, Hq, Hkv, hd, 1.0f / sqrtf((float)hd)};
-        const int sm = att_smem_bytes<__nv_bfloat16>(hd);
+        const int sm = att_smem_bytes<__nv_bfloat16>(hd, Hq / Hkv);
         cudaFuncSetAttribute(k_attn_direct<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
         k_attn_direct<__nv_bfloat16><<<grid, ATT_THREADS, sm, s>>>(a);
     } else {
         AttnArgs<float> a{q, nullptr, nullptr, nullptr, const_cast<float *>(reinterpret_cast<const float *>(k)),
                           const_cast<float *>(reinterpret_cast<const float *>(v)), seq_len, out, part, cnt, 0, nch, Hq,
                           Hkv, hd, 1.0f / sqrtf((float)hd)};
-        const int sm = att_smem_bytes<float>(hd);
+        const int sm = att_smem_bytes<float>(hd, Hq / Hkv);
         cudaFuncSetAttribute(k_attn_direct<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
         k_attn_direct<float><<<grid, ATT_THREADS, sm, s>>>(a);
     }

@@ -10,25 +10,51 @@
 // the in-flight tokens, at consecutive positions, so its attention is plain causal
 // attention over its own cache.
 //
-// Every GEMM here multiplies one weight matrix by R <= n+1 row vectors (a skinny
-// GEMM), so it runs on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
-// the weights are the M side streamed straight from HBM with 16-byte loads, the R
-// activation rows (bf16 in shared memory) the N side.  The K dimension of one
-// product is kept in a permuted order that is the same for both operands, so each
-// lane's 16-byte weight load feeds the A fragment directly.  K is split over CTAs; the
-// last CTA of a 128-row block adds the partial sums in split order (deterministic) and
-// runs the epilogue (RoPE + KV append, residual add, ...); the last block overall
-// recomputes the rows' RMS statistics for the next normalisation.
+// Every GEMM here multiplies one weight matrix W [N][K] by R <= n+1 row vectors x [R][K]
+// (a skinny GEMM: far more bytes of W than of x, so it is bound by streaming W once from
+// HBM).  Design, one CTA per SM:
+//   * a producer warp streams 8-row tiles of W (each row piece up to 6 KB, 1-D bulk copies)
+//     into a shared-memory ring signalled by mbarriers, as the target's GEMVs do;
+//   * the R rows of x are staged once per launch in shared memory as bf16 (or fp32 for
+//     fp32 weights), with the input's normalisation / SiLU-product / anchor masking fused
+//     into the staging;
+//   * the 8 consumer warps split each tile's K range into 32-element blocks (block b to
+//     warp b mod 8); per block a warp runs two m16n8k16 tensor-core steps with the x rows
+//     as the 16-row A operand and the 8 weight rows as the B operand.  Both operands take
+//     K in the same permuted order inside the block, so one 16-byte shared-memory read
+//     per lane feeds a whole fragment;
+//   * after the last K piece of a tile group the warps' partial 16x8 products meet in
+//     shared memory and are added in warp order (deterministic), then the epilogue writes
+//     or accumulates the outputs.
+// A K range whose x rows do not fit in shared memory beside the ring is cut into slabs,
+// one launch each; later slabs add into the output in slab order.
+// RoPE and the append of the rows' K,V to the module's cache run in a small kernel
+// between the QKV GEMM and attention (the rows' attention depends on one another's K,V).
 #include "common.cuh"
 
 namespace spd {
 
-enum { XM_FEAT = 0, XM_NORM1, XM_NORM2, XM_ATT, XM_SILU };
-enum { SE_PROJ = 0, SE_QKV, SE_OPROJ, SE_GATEUP, SE_DOWN };
-constexpr int SK_THREADS = 256;
+enum { OP_PROJ = 0, OP_QKV, OP_OPROJ, OP_GATEUP, OP_DOWN };
 
-template <typename T> struct SkX { using type = float; };
-template <> struct SkX<__nv_bfloat16> { using type = __nv_bfloat16; };
+constexpr int PG_CONSUMERS = 256;              // 8 consumer warps
+constexpr int PG_THREADS = PG_CONSUMERS + 32;  // + 1 producer warp
+constexpr int PG_RG = 8;                       // weight rows per tile (the mma's n)
+constexpr int PG_ROWB = 6144;                  // bytes of one row per tile piece, at most
+constexpr int PG_MAXNS = 8;                    // ring stages at most
+constexpr int PG_SMEM = 210 * 1024;            // x + reduction buffers + ring
+constexpr int PG_XMAX = 96 * 1024;             // budget of the x rows of one slab
+constexpr int PG_KB = 32;                      // K elements per warp block
+constexpr int PG_BAR = 1;                      // named barrier of the consumer warps
+
+__host__ __device__ inline int pg_round(int v, int m) { return (v + m - 1) / m * m; }
+// row pitch (bytes) of x and of a weight tile: 128-byte multiple + 64, so the 8 rows that
+// one fragment read touches fall alternately into the two halves of the banks
+__host__ __device__ inline int pg_pitch(int elems, int esz) { return pg_round(elems * esz, 128) + 64; }
+__host__ __device__ inline int pg_xbytes(int rows, int kx, int esz) { return pg_round(rows * pg_pitch(kx, esz), 128); }
+__host__ __device__ inline int pg_redbytes(int MT) { return 2 * (PG_CONSUMERS / 32) * MT * 32 * 16; }
+// K pieces of one slab of kw elements: nch pieces of KC elements (multiples of PG_KB)
+__host__ __device__ inline int pg_nch(int kw, int esz) { return (kw * esz + PG_ROWB - 1) / PG_ROWB; }
+__host__ __device__ inline int pg_kc(int kw, int esz) { return pg_round((kw + pg_nch(kw, esz) - 1) / pg_nch(kw, esz), PG_KB); }
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -38,371 +64,440 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_u32(p)));
+    return r;
+}
 
-template <typename T, int SE>
-__device__ __forceinline__ const T *sk_row(const Plan *__restrict__ P, int layer, int row, int K) {
-    if (SE == SE_PROJ) return reinterpret_cast<const T *>(P->proj) + (long long)row * K;
+template <int OP> __host__ __device__ inline int pg_N(const Plan &h) {
+    return OP == OP_QKV ? h.qkv_rows : OP == OP_GATEUP ? 2 * h.F : h.d;
+}
+template <int OP> __host__ __device__ inline int pg_K(const Plan &h) {
+    return OP == OP_PROJ ? h.nB * h.d : OP == OP_OPROJ ? h.q_rows : OP == OP_DOWN ? h.F : h.d;
+}
+
+// Weight rows of one GEMM: row u is row u of region 0 below b1, row u - b1 of region 1
+// below b2, else row u - b2 of region 2.
+template <typename T>
+struct PgRows {
+    const T *p0, *p1, *p2;
+    int b1, b2, K;
+    __device__ __forceinline__ const T *row(int u) const {
+        if (u < b1) return p0 + (long long)u * K;
+        if (u < b2) return p1 + (long long)(u - b1) * K;
+        return p2 + (long long)(u - b2) * K;
+    }
+};
+template <typename T, int OP>
+__device__ __forceinline__ PgRows<T> pg_rows(const Plan *__restrict__ P, int layer, int K) {
+    PgRows<T> r;
+    r.K = K;
+    r.b1 = r.b2 = 0x7fffffff;
+    r.p1 = r.p2 = nullptr;
+    if (OP == OP_PROJ) {
+        r.p0 = reinterpret_cast<const T *>(P->proj);
+        return r;
+    }
     const LayerW &w = P->pl[layer];
-    if (SE == SE_QKV) {
-        if (row < P->q_rows) return reinterpret_cast<const T *>(w.wq) + (long long)row * K;
-        row -= P->q_rows;
-        if (row < P->kv_rows) return reinterpret_cast<const T *>(w.wk) + (long long)row * K;
-        return reinterpret_cast<const T *>(w.wv) + (long long)(row - P->kv_rows) * K;
+    if (OP == OP_QKV) {
+        r.p0 = reinterpret_cast<const T *>(w.wq);
+        r.p1 = reinterpret_cast<const T *>(w.wk);
+        r.p2 = reinterpret_cast<const T *>(w.wv);
+        r.b1 = P->q_rows;
+        r.b2 = P->q_rows + P->kv_rows;
+    } else if (OP == OP_GATEUP) {
+        r.p0 = reinterpret_cast<const T *>(w.wg);
+        r.p1 = reinterpret_cast<const T *>(w.wu);
+        r.b1 = P->F;
+    } else {
+        r.p0 = reinterpret_cast<const T *>(OP == OP_OPROJ ? w.wo : w.wd);
     }
-    if (SE == SE_OPROJ) return reinterpret_cast<const T *>(w.wo) + (long long)row * K;
-    if (SE == SE_GATEUP) {
-        if (row < P->F) return reinterpret_cast<const T *>(w.wg) + (long long)row * K;
-        return reinterpret_cast<const T *>(w.wu) + (long long)(row - P->F) * K;
-    }
-    return reinterpret_cast<const T *>(w.wd) + (long long)row * K;
+    return r;
 }
 
-template <int XM>
-__device__ __forceinline__ float sk_xval(const Plan *__restrict__ P, const PdmRows &pr, int layer, int r, int k) {
-    const int d = P->d;
-    if (XM == XM_FEAT) {
-        const int a = k / d, off = k - a * d;
-        if (P->anchors[a] > pr.depth[r]) return 0.f;
-        return P->ANCH[((long long)pr.slot[r] * P->nB + a) * d + off];
+// ---- x staging (consumer warps only) ---------------------------------------------------
+// x row r, slab-relative columns [0, kw): element k of the GEMM's input at k0 + k.
+template <typename XT>
+__device__ __forceinline__ void pg_store4(unsigned char *xs, int pitch, int r, int k, float4 v) {
+    if (sizeof(XT) == 2) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&a);
+        u.y = *reinterpret_cast<uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(xs + r * pitch + k * 2) = u;
+    } else {
+        *reinterpret_cast<float4 *>(xs + r * pitch + k * 4) = v;
     }
-    if (XM == XM_NORM1 || XM == XM_NORM2) {
-        const float *g = XM == XM_NORM1 ? P->pl[layer].g1 : P->pl[layer].g2;
-        return (P->Xp[(long long)r * d + k] * P->inv_rms_p[r]) * g[k];
-    }
-    if (XM == XM_ATT) return P->ATTp[(long long)r * P->q_rows + k];
-    const float gg = P->GUp[(long long)r * 2 * P->F + k];
-    const float uu = P->GUp[(long long)r * 2 * P->F + P->F + k];
-    return silu_f(gg) * uu;
 }
 
-template <typename T, int NT, int XM, int SE>
-__global__ void __launch_bounds__(SK_THREADS) k_skinny(const Plan *__restrict__ P, int layer, int N, int K, int nks) {
-    using XT = typename SkX<T>::type;
-    constexpr int RP = NT * 8;
-    extern __shared__ __align__(16) unsigned char sk_smem[];
+// Per-row RMS statistics of Xp rows 0..R-1 from the per-CTA sums of squares that the
+// kernel which last wrote Xp left in ssp (CTA order, then a fixed shuffle tree).
+__device__ __noinline__ void pg_row_inv_rms(const Plan *__restrict__ P, int R, float *inv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, G = P->pdm_grid;
+    for (int r = warp; r < R; r += PG_CONSUMERS / 32) {
+        float s = 0.f;
+        for (int c = lane; c < G; c += 32) s += P->ssp[c * MAXS + r];
+        s = warp_sum(s);
+        if (lane == 0) inv[r] = 1.0f / sqrtf(s / (float)P->d + P->eps);
+    }
+}
+
+// Stage the slab of all R rows: items are 4-element groups, 8 in flight per thread.
+template <typename XT, int OP>
+__device__ __noinline__ void pg_stage_x(const Plan *__restrict__ P, const PdmRows &pr, int layer, int k0, int kw,
+                                        unsigned char *xs, int pitch, const float *inv) {
+    const int R = pr.R, kw4 = kw >> 2, total = R * kw4, d = P->d;
+    const float *g = OP == OP_QKV ? P->pl[layer].g1 : OP == OP_GATEUP ? P->pl[layer].g2 : nullptr;
+    for (int b = threadIdx.x; b < total; b += 8 * PG_CONSUMERS) {
+        float4 v[8], w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * PG_CONSUMERS;
+            if (i >= total) continue;
+            const int r = i / kw4, k = k0 + 4 * (i - r * kw4);
+            if (OP == OP_PROJ) {
+                const int a = k / d, off = k - a * d;
+                v[u] = P->anchors[a] <= pr.depth[r]
+                           ? *reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + a) * d + off)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (OP == OP_QKV || OP == OP_GATEUP) {
+                v[u] = *reinterpret_cast<const float4 *>(P->Xp + (long long)r * d + k);
+                w[u] = *reinterpret_cast<const float4 *>(g + k);
+            } else if (OP == OP_OPROJ) {
+                v[u] = *reinterpret_cast<const float4 *>(P->ATTp + (long long)r * P->q_rows + k);
+            } else {
+                v[u] = *reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + k);
+                w[u] = *reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + P->F + k);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * PG_CONSUMERS;
+            if (i >= total) continue;
+            const int r = i / kw4, kk = 4 * (i - r * kw4);
+            float4 x = v[u];
+            if (OP == OP_QKV || OP == OP_GATEUP) {
+                const float s = inv[r];
+                x = make_float4((x.x * s) * w[u].x, (x.y * s) * w[u].y, (x.z * s) * w[u].z, (x.w * s) * w[u].w);
+            } else if (OP == OP_DOWN) {
+                x = make_float4(silu_f(x.x) * w[u].x, silu_f(x.y) * w[u].y, silu_f(x.z) * w[u].z, silu_f(x.w) * w[u].w);
+            }
+            pg_store4<XT>(xs, pitch, r, kk, x);
+        }
+    }
+}
+
+// ---- the GEMM ---------------------------------------------------------------------------
+// Output rows [lo, hi) of this CTA in groups of 8; slab [k0, k0 + kw) of K, kw = min(kx, K - k0).
+template <typename T, int OP, int MT>
+__global__ void __launch_bounds__(PG_THREADS, 1) k_pdm_gemm(const Plan *__restrict__ P, int layer, int k0, int kx) {
+    using XT = T;   // x rows are kept in the weights' type (bf16 operands for the tensor cores)
+    constexpr int ESZ = sizeof(T);
+    extern __shared__ __align__(128) unsigned char pg_smem[];
+    __shared__ __align__(8) uint64_t full[PG_MAXNS], empty[PG_MAXNS];
     __shared__ PdmRows pr;
-    __shared__ int s_done, s_last, s_glast;
-    if (threadIdx.x < 32) warp_pdm_rows(P, pr, &s_done);
-    __syncthreads();
-    if (s_done) return;
-    const int R = pr.R;
-    const int nrb = (N + SK_ROWS - 1) / SK_ROWS;
-    const int rb = blockIdx.x / nks, ks = blockIdx.x % nks;
-    const int nch = K / SK_KCHUNK;
-    const int c0 = (int)((long long)nch * ks / nks), c1 = (int)((long long)nch * (ks + 1) / nks);
-    const int k0 = c0 * SK_KCHUNK, kseg = (c1 - c0) * SK_KCHUNK;
-    const int kmax = ((nch + nks - 1) / nks) * SK_KCHUNK;
-    const int pitch = kmax + (sizeof(XT) == 2 ? 32 : 4);   // elements; keeps 16-byte rows off one bank
-    XT *xs = reinterpret_cast<XT *>(sk_smem);
-
-    // ---- stage the R activation rows of this K segment (8 loads in flight per thread)
-    const int total = RP * kseg;
-    for (int b = threadIdx.x; b < total; b += 8 * blockDim.x) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = b + u * blockDim.x;
-            const int r = idx / kseg, kk = idx - r * kseg;
-            v[u] = (idx < total && r < R) ? sk_xval<XM>(P, pr, layer, r, k0 + kk) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int idx = b + u * blockDim.x;
-            if (idx >= total) continue;
-            const int r = idx / kseg, kk = idx - r * kseg;
-            if (sizeof(XT) == 2)
-                reinterpret_cast<__nv_bfloat16 *>(xs)[r * pitch + kk] = __float2bfloat16_rn(v[u]);
-            else
-                reinterpret_cast<float *>(xs)[r * pitch + kk] = v[u];
+    __shared__ float s_inv[MAXS];
+    __shared__ int s_done;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        warp_pdm_rows(P, pr, &s_done);
+        if (lane == 0) {
+            for (int i = 0; i < PG_MAXNS; ++i) {
+                mbar_init(&full[i], 1);
+                mbar_init(&empty[i], PG_CONSUMERS / 32);
+            }
+            fence_mbar_init();
         }
     }
     __syncthreads();
+    if (s_done || pr.R < 1) return;
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int rbase = rb * SK_ROWS + warp * 16;
-    float *part = P->sk_part;
-    if constexpr (sizeof(XT) == 2) {
-        // tensor-core engine
-        const int gq = lane >> 2, tq = lane & 3;
-        const int ra = min(rbase + gq, N - 1), rc = min(rbase + gq + 8, N - 1);
-        const T *wa = sk_row<T, SE>(P, layer, ra, K) + k0 + 8 * tq;
-        const T *wc = sk_row<T, SE>(P, layer, rc, K) + k0 + 8 * tq;
-        float acc[NT][4];
+    const int N = pg_N<OP>(*P), K = pg_K<OP>(*P);
+    const int kw = min(kx, K - k0);
+    const int nch = pg_nch(kw, ESZ), KC = pg_kc(kw, ESZ);
+    const int xpitch = pg_pitch(kx, ESZ);
+    const int rowb = pg_pitch(KC, ESZ), stage_bytes = PG_RG * rowb;
+    const int xbytes = pg_xbytes(P->n + 1, kx, ESZ);
+    unsigned char *xs = pg_smem;
+    float4 *red = reinterpret_cast<float4 *>(pg_smem + xbytes);
+    unsigned char *stages = pg_smem + xbytes + pg_redbytes(MT);
+    const int NS = min(PG_MAXNS, (PG_SMEM - xbytes - pg_redbytes(MT)) / stage_bytes);
+    const int lo = (int)((long long)N * blockIdx.x / gridDim.x);
+    const int hi = (int)((long long)N * (blockIdx.x + 1) / gridDim.x);
+
+    if (warp == PG_CONSUMERS / 32) {
+        // ------------------------------ producer ----------------------------------------
+        if (lane == 0) {
+            const PgRows<T> wr = pg_rows<T, OP>(P, layer, K);
+            uint32_t tile = 0;
+            for (int g0 = lo; g0 < hi; g0 += PG_RG) {
+                const T *rp[PG_RG];
+                int nrows = 0;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(xs) + 8 * tq;
-        const bool active = rbase < N;
-        int kk = 0;
-        if (active) {
-            for (; kk + 2 * SK_KCHUNK <= kseg; kk += 2 * SK_KCHUNK) {
-                uint4 A[2][4];
+                for (int q = 0; q < PG_RG; ++q) {
+                    rp[q] = g0 + q < hi ? wr.row(g0 + q) + k0 : nullptr;
+                    nrows += rp[q] != nullptr;
+                }
+                for (int c = 0; c < nch; ++c) {
+                    const int kc0 = c * KC, len = min(KC, kw - kc0);
+                    const int sidx = tile % NS;
+                    const uint32_t u = tile / NS;
+                    if (!mbar_wait(&empty[sidx], (u & 1) ^ 1)) P->st->error = ERR_TIMEOUT;
+                    const uint32_t bytes = (uint32_t)len * ESZ;
+                    mbar_expect_tx(&full[sidx], bytes * nrows);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    A[h][0] = ld_stream(wa + kk + h * SK_KCHUNK);
-                    A[h][1] = ld_stream(wc + kk + h * SK_KCHUNK);
-                    A[h][2] = ld_stream(wa + kk + h * SK_KCHUNK + 32);
-                    A[h][3] = ld_stream(wc + kk + h * SK_KCHUNK + 32);
+                    for (int q = 0; q < PG_RG; ++q)
+                        if (rp[q]) bulk_g2s(stages + sidx * stage_bytes + q * rowb, rp[q] + kc0, bytes, &full[sidx]);
+                    ++tile;
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------ consumers -------------------------------------------
+    const int tid = threadIdx.x, R = pr.R;
+    if (OP == OP_QKV || OP == OP_GATEUP) {
+        pg_row_inv_rms(P, R, s_inv);
+        named_sync(PG_BAR, PG_CONSUMERS);
+    }
+    pg_stage_x<XT, OP>(P, pr, layer, k0, kw, xs, xpitch, s_inv);
+    named_sync(PG_BAR, PG_CONSUMERS);
+
+    // output of one (x row, weight row) pair
+    const int d = P->d;
+    float *dst;
+    int ld;
+    bool accum;
+    if (OP == OP_QKV) {
+        dst = P->QKVp; ld = P->qkv_rows; accum = k0 > 0;
+    } else if (OP == OP_GATEUP) {
+        dst = P->GUp; ld = 2 * P->F; accum = k0 > 0;
+    } else {
+        dst = P->Xp; ld = d; accum = OP != OP_PROJ || k0 > 0;
+    }
+
+    // kernels that finish an Xp row (the last slab of proj / o / down) leave per-CTA sums of
+    // squares for the next normalisation; reduction thread t always owns the same
+    // (x row, weight row) pair of a group, so it sums its squares over the groups in order
+    const bool want_ss = (OP == OP_PROJ || OP == OP_OPROJ || OP == OP_DOWN) && k0 + kw == K;
+    float sq = 0.f;
+    const int gq = lane >> 2, tq = lane & 3;
+    uint32_t tile = 0;
+    int buf = 0;
+    for (int g0 = lo; g0 < hi; g0 += PG_RG) {
+        // bf16: acc[4m..4m+3] is the m-th 16x8 mma accumulator fragment; fp32: acc[j] is the
+        // (x row (lane >> 3) + 4j, weight row lane & 7) product
+        float acc[4 * MT];
+#pragma unroll
+        for (int j = 0; j < 4 * MT; ++j) acc[j] = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const int kc0 = c * KC, len = min(KC, kw - kc0), nblk = len / PG_KB;
+            const int sidx = tile % NS;
+            const uint32_t u = tile / NS;
+            if (!mbar_wait(&full[sidx], u & 1)) P->st->error = ERR_TIMEOUT;
+            const unsigned char *tb = stages + sidx * stage_bytes;
+            if constexpr (ESZ == 2) {
+                // lane (gq, tq): weight row gq, x rows gq and gq + 8 (+16 m), elements 8tq..8tq+7 of
+                // each 32-block; the two mma steps take elements {8tq..8tq+3} and {8tq+4..8tq+7}
+                const unsigned char *wp = tb + gq * rowb + tq * 16;
+                const unsigned char *xp = xs + gq * xpitch + kc0 * 2 + tq * 16;
+                bool xv[MT][2];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    xv[m][0] = m * 16 + gq < R;
+                    xv[m][1] = m * 16 + 8 + gq < R;
+                }
+                // the two mma steps of a block go to two accumulator chains (added at the end of
+                // the piece, fixed order)
+                float acc2[4 * MT];
+#pragma unroll
+                for (int j = 0; j < 4 * MT; ++j) acc2[j] = 0.f;
+                for (int b = warp; b < nblk; b += PG_CONSUMERS / 32) {
+                    const uint4 w = lds128(wp + b * 64);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 xa = xv[m][0] ? lds128(xp + (m * 16) * xpitch + b * 64) : z;
+                        const uint4 xb = xv[m][1] ? lds128(xp + (m * 16 + 8) * xpitch + b * 64) : z;
+                        float(&f)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * m]);
+                        float(&f2)[4] = *reinterpret_cast<float(*)[4]>(&acc2[4 * m]);
+                        mma_bf16(f, xa.x, xb.x, xa.y, xb.y, w.x, w.y);
+                        mma_bf16(f2, xa.z, xb.z, xa.w, xb.w, w.z, w.w);
+                    }
                 }
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int j = 0; j < 4 * MT; ++j) acc[j] += acc2[j];
+            } else {
+                // fp32 weights: plain FMAs in element order
+                const int wrow = lane & 7, xq = lane >> 3;
+                const float *wp = reinterpret_cast<const float *>(tb + wrow * rowb);
+                for (int b = warp; b < nblk; b += PG_CONSUMERS / 32) {
+                    for (int e = 0; e < PG_KB; ++e) {
+                        const int k = b * PG_KB + e;
+                        const float wv = wp[k];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const __nv_bfloat16 *xr = xb + (nt * 8 + gq) * pitch + kk + h * SK_KCHUNK;
-                        const uint4 b0 = *reinterpret_cast<const uint4 *>(xr);
-                        const uint4 b1 = *reinterpret_cast<const uint4 *>(xr + 32);
-                        mma_bf16(acc[nt], A[h][0].x, A[h][1].x, A[h][0].y, A[h][1].y, b0.x, b0.y);
-                        mma_bf16(acc[nt], A[h][0].z, A[h][1].z, A[h][0].w, A[h][1].w, b0.z, b0.w);
-                        mma_bf16(acc[nt], A[h][2].x, A[h][3].x, A[h][2].y, A[h][3].y, b1.x, b1.y);
-                        mma_bf16(acc[nt], A[h][2].z, A[h][3].z, A[h][2].w, A[h][3].w, b1.z, b1.w);
+                        for (int j = 0; j < 4 * MT; ++j) {
+                            const int xr = xq + 4 * j;
+                            if (xr < R) acc[j] = fmaf(wv, reinterpret_cast<const float *>(xs + xr * xpitch)[kc0 + k], acc[j]);
+                        }
                     }
                 }
             }
-            for (; kk < kseg; kk += SK_KCHUNK) {
-                const uint4 a0 = ld_stream(wa + kk), a1 = ld_stream(wc + kk);
-                const uint4 a2 = ld_stream(wa + kk + 32), a3 = ld_stream(wc + kk + 32);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sidx]);
+            ++tile;
+        }
+        // ---- partial products of all warps -> fixed-order sum -> epilogue
+        // shared buffer in the mma fragment layout: [buf][warp][m][lane] x 4 floats, float
+        // (m, lane, reg) = product (x row 16m + 8(reg >> 1) + lane / 4, weight row 2(lane % 4) + reg % 2)
+        if constexpr (ESZ == 2) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const __nv_bfloat16 *xr = xb + (nt * 8 + gq) * pitch + kk;
-                    const uint4 b0 = *reinterpret_cast<const uint4 *>(xr);
-                    const uint4 b1 = *reinterpret_cast<const uint4 *>(xr + 32);
-                    mma_bf16(acc[nt], a0.x, a1.x, a0.y, a1.y, b0.x, b0.y);
-                    mma_bf16(acc[nt], a0.z, a1.z, a0.w, a1.w, b0.z, b0.w);
-                    mma_bf16(acc[nt], a2.x, a3.x, a2.y, a3.y, b1.x, b1.y);
-                    mma_bf16(acc[nt], a2.z, a3.z, a2.w, a3.w, b1.z, b1.w);
-                }
-            }
-            // D fragment: (row gq, cols 2tq, 2tq+1) and (row gq+8, same cols)
+            for (int m = 0; m < MT; ++m)
+                red[((buf * (PG_CONSUMERS / 32) + warp) * MT + m) * 32 + lane] =
+                    make_float4(acc[4 * m], acc[4 * m + 1], acc[4 * m + 2], acc[4 * m + 3]);
+        } else {
+            float *rf = reinterpret_cast<float *>(red);
+            const int wrow = lane & 7, xq = lane >> 3;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int col = nt * 8 + 2 * tq;
-                const int r0 = rbase + gq, r1 = rbase + gq + 8;
-                if (r0 < N) {
-                    part[((long long)ks * N + r0) * RP + col] = acc[nt][0];
-                    part[((long long)ks * N + r0) * RP + col + 1] = acc[nt][1];
-                }
-                if (r1 < N) {
-                    part[((long long)ks * N + r1) * RP + col] = acc[nt][2];
-                    part[((long long)ks * N + r1) * RP + col + 1] = acc[nt][3];
-                }
+            for (int j = 0; j < 4 * MT; ++j) {
+                const int xr = xq + 4 * j, m = xr >> 4, r16 = xr & 15;
+                const int l2 = (r16 & 7) * 4 + (wrow >> 1), reg = (r16 >> 3) * 2 + (wrow & 1);
+                rf[(((buf * (PG_CONSUMERS / 32) + warp) * MT + m) * 32 + l2) * 4 + reg] = acc[j];
             }
+        }
+        named_sync(PG_BAR, PG_CONSUMERS);
+        if (tid < 128 * MT) {
+            const int m = tid >> 7, l = (tid >> 2) & 31, reg = tid & 3;
+            const float *rf = reinterpret_cast<const float *>(red);
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < PG_CONSUMERS / 32; ++w) s += rf[(((buf * (PG_CONSUMERS / 32) + w) * MT + m) * 32 + l) * 4 + reg];
+            const int xr = m * 16 + (reg >> 1) * 8 + (l >> 2);
+            const int row = g0 + (l & 3) * 2 + (reg & 1);
+            if (xr < R && row < hi) {
+                float *o = dst + (long long)xr * ld + row;
+                const float v = accum ? *o + s : s;
+                *o = v;
+                sq = fmaf(v, v, sq);
+            }
+        }
+        buf ^= 1;
+    }
+    if (want_ss && tid < 128 * MT) {
+        // the 8 weight rows of one x row sit in lanes differing in bits 0, 2 and 3 of tid
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 4);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+        const int m = tid >> 7, l = (tid >> 2) & 31, reg = tid & 3;
+        if ((tid & 13) == 0) P->ssp[blockIdx.x * MAXS + m * 16 + (reg >> 1) * 8 + (l >> 2)] = sq;
+    }
+}
+
+// ---- RoPE of q and k, and the rows' K,V into the module's cache ---------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) k_pdm_rope_kv(const Plan *__restrict__ P, int layer) {
+    __shared__ PdmRows pr;
+    __shared__ int s_done;
+    if (threadIdx.x < 32) warp_pdm_rows(P, pr, &s_done);
+    __syncthreads();
+    const int r = blockIdx.x;
+    if (s_done || r >= pr.R) return;
+    // items: q pairs, k pairs (rotate-half RoPE at the row's position), then v elements
+    const int hd = P->hd, half = hd >> 1, pos = pr.pos0 + r;
+    const int nq = P->Hq * half, nk = P->Hkv * half, i = blockIdx.y * blockDim.x + threadIdx.x;
+    if (i >= nq + nk + P->kv_rows) return;
+    float *q = P->QKVp + (long long)r * P->qkv_rows;
+    const long long off = (long long)layer * P->kv_stride + (long long)pos * P->kv_rows;
+    if (i < nq + nk) {
+        const int ii = i < nq ? i : i - nq;
+        const int h = ii / half, j = ii - h * half;
+        float *src = (i < nq ? q : q + P->q_rows) + h * hd + j;
+        const float2 c = P->rope[(long long)pos * half + j];
+        const float a = src[0], b = src[half];
+        const float y0 = a * c.x - b * c.y, y1 = b * c.x + a * c.y;
+        if (i < nq) {
+            src[0] = y0;
+            src[half] = y1;
+        } else {
+            T *kc = reinterpret_cast<T *>(P->pkc) + off + h * hd + j;
+            kc[0] = WTraits<T>::store(y0);
+            kc[half] = WTraits<T>::store(y1);
         }
     } else {
-        // fp32 engine (fp32 weights): one row at a time, lanes split K
-        const float *xf = reinterpret_cast<const float *>(xs);
-        for (int rr = 0; rr < 16; ++rr) {
-            const int row = rbase + rr;
-            if (row >= N) break;
-            const T *w = sk_row<T, SE>(P, layer, row, K) + k0;
-            float acc[RP];
-#pragma unroll
-            for (int r = 0; r < RP; ++r) acc[r] = 0.f;
-            for (int k = lane; k < kseg; k += 32) {
-                const float wv = (float)w[k];
-#pragma unroll
-                for (int r = 0; r < RP; ++r) acc[r] = fmaf(wv, xf[r * pitch + k], acc[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                const float s = warp_sum(acc[r]);
-                if (lane == 0) part[((long long)ks * N + row) * RP + r] = s;
-            }
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(P->sk_cnt + rb, 1) == nks - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    // ---- epilogue for rows [rb*128, rb*128+128): sum the K-split partials in split order.
-    // Each thread owns items tid, tid+256, ...; the loads of 4 items x 8 splits are issued
-    // before any add, so the chain costs a few L2 round trips, not nks of them.
-    const int rlo = rb * SK_ROWS, rhi = min(N, rlo + SK_ROWS);
-    const int d = P->d;
-    float *ys = reinterpret_cast<float *>(sk_smem);   // [128][RP] (reuses the x buffer)
-    __syncthreads();
-    const int nitems = (rhi - rlo) * R;
-    for (int i0 = threadIdx.x; i0 < nitems; i0 += 4 * blockDim.x) {
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-        long long base[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int idx = min(i0 + e * (int)blockDim.x, nitems - 1);
-            const int rl = idx / R, r = idx - rl * R;
-            base[e] = (long long)(rlo + rl) * RP + r;
-        }
-        for (int q0 = 0; q0 < nks; q0 += 8) {
-            float v[4][8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    v[e][u] = (i0 + e * (int)blockDim.x < nitems && q0 + u < nks)
-                                  ? __ldcg(part + (long long)(q0 + u) * N * RP + base[e]) : 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (q0 + u < nks) sum[e] += v[e][u];
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int idx = i0 + e * blockDim.x;
-            if (idx >= nitems) continue;
-            const int rl = idx / R, r = idx - rl * R;
-            const int row = rlo + rl;
-            if (SE == SE_PROJ) P->Xp[(long long)r * d + row] = sum[e];
-            else if (SE == SE_OPROJ || SE == SE_DOWN) P->Xp[(long long)r * d + row] += sum[e];
-            else if (SE == SE_GATEUP) P->GUp[(long long)r * 2 * P->F + row] = sum[e];
-            else ys[rl * RP + r] = sum[e];
-        }
-    }
-    if (SE == SE_QKV) {
-        __syncthreads();
-        const int hd = P->hd, half = hd / 2, Hkv = P->Hkv;
-        const long long rowstride = (long long)Hkv * hd;
-        T *kc = reinterpret_cast<T *>(P->pkc) + (long long)layer * P->kv_stride;
-        T *vc = reinterpret_cast<T *>(P->pvc) + (long long)layer * P->kv_stride;
-        for (int idx = threadIdx.x; idx < (rhi - rlo) * R; idx += blockDim.x) {
-            const int rl = idx / R, r = idx - rl * R;
-            const int row = rlo + rl;
-            const int pos = pr.pos0 + r;
-            const int i = row % hd;
-            if (row < P->q_rows + P->kv_rows) {
-                // q or k: rotate-half RoPE at the row's position
-                const int ii = i < half ? i : i - half;
-                const float2 cs = P->rope[(long long)pos * half + ii];
-                const float a = ys[(rl - i + ii) * RP + r], b = ys[(rl - i + ii + half) * RP + r];
-                const float v = i < half ? a * cs.x - b * cs.y : b * cs.x + a * cs.y;
-                if (row < P->q_rows)
-                    P->QKVp[(long long)r * P->qkv_rows + row] = v;
-                else {
-                    const int kr = row - P->q_rows;
-                    kc[(long long)pos * rowstride + kr] = WTraits<T>::store(v);
-                }
-            } else {
-                const int vr = row - P->q_rows - P->kv_rows;
-                vc[(long long)pos * rowstride + vr] = WTraits<T>::store(ys[rl * RP + r]);
-            }
-        }
-    }
-    if (threadIdx.x == 0) P->sk_cnt[rb] = 0;
-    if (SE == SE_PROJ || SE == SE_OPROJ || SE == SE_DOWN) {
-        // last block overall: RMS statistics of the updated rows for the next norm
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) s_glast = atomicAdd(P->sk_cnt + nrb, 1) == nrb - 1;
-        __syncthreads();
-        if (!s_glast) return;
-        __threadfence();
-        // all rows at once: per-thread sums of squares with the rows' loads in flight
-        // together, then one fixed-order reduction over warps per row
-        float ss[RP];
-#pragma unroll
-        for (int r = 0; r < RP; ++r) ss[r] = 0.f;
-        for (int k = threadIdx.x; k < d; k += blockDim.x) {
-#pragma unroll
-            for (int r = 0; r < RP; ++r)
-                if (r < R) {
-                    const float v = __ldcg(P->Xp + (long long)r * d + k);
-                    ss[r] = fmaf(v, v, ss[r]);
-                }
-        }
-        float *wred = reinterpret_cast<float *>(sk_smem);   // [8 warps][RP]
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            const float t = warp_sum(ss[r]);
-            if (lane == 0) wred[warp * RP + r] = t;
-        }
-        __syncthreads();
-        if (threadIdx.x < R) {
-            float t = 0.f;
-            for (int w = 0; w < SK_THREADS / 32; ++w) t += wred[w * RP + threadIdx.x];
-            P->inv_rms_p[threadIdx.x] = 1.0f / sqrtf(t / (float)d + P->eps);
-        }
-        if (threadIdx.x == 0) P->sk_cnt[nrb] = 0;
+        const int e = i - nq - nk;
+        reinterpret_cast<T *>(P->pvc)[off + e] = WTraits<T>::store(q[P->q_rows + P->kv_rows + e]);
     }
 }
 
 // ---------------------------------------------------------------------------------
-static int sk_smem_for(const Plan &h, int K, int nks, int NT, int xbytes) {
-    const int nch = K / SK_KCHUNK;
-    const int kmax = ((nch + nks - 1) / nks) * SK_KCHUNK;
-    const int pitch = kmax + (xbytes == 2 ? 32 : 4);
-    int b = NT * 8 * pitch * xbytes;
-    const int ys = SK_ROWS * NT * 8 * 4;
-    return b > ys ? b : ys;
+// Host side: slab width per GEMM so that the x rows of one slab fit their budget.
+static int pg_slab(int K, int rows, int esz) {
+    int kx = pg_round(K, PG_KB);
+    int ns = 1;
+    while (pg_xbytes(rows, kx, esz) > PG_XMAX) {
+        ++ns;
+        kx = pg_round((K + ns - 1) / ns, PG_KB);
+    }
+    return kx;
 }
 
-void sk_plan(const Plan &h, int num_sms, SkPlan &sk) {
-    const int Ns[5] = {h.d, h.qkv_rows, h.d, 2 * h.F, h.d};
-    const int Ks[5] = {h.nB * h.d, h.d, h.q_rows, h.d, h.F};
-    sk.NT = (h.n + 1 + 7) / 8;
-    const int xbytes = h.dtype == SPD_BF16 ? 2 : 4;
-    sk.smem = 0;
+void pdm_plan(const Plan &h, PdmPlan &pp) {
+    const int esz = h.dtype == SPD_BF16 ? 2 : 4, rows = h.n + 1;
+    pp.MT = rows <= 16 ? 1 : 2;
+    const int Ks[5] = {pg_K<OP_PROJ>(h), pg_K<OP_QKV>(h), pg_K<OP_OPROJ>(h), pg_K<OP_GATEUP>(h), pg_K<OP_DOWN>(h)};
     for (int i = 0; i < 5; ++i) {
-        const int nrb = (Ns[i] + SK_ROWS - 1) / SK_ROWS;
-        const int nch = Ks[i] / SK_KCHUNK;
-        int nks = (2 * num_sms + nrb - 1) / nrb;
-        if (nks < 1) nks = 1;
-        if (nks > nch) nks = nch;
-        sk.nks[i] = nks;
-        const int sm = sk_smem_for(h, Ks[i], nks, sk.NT, xbytes);
-        if (sm > sk.smem) sk.smem = sm;
+        pp.kx[i] = pg_slab(Ks[i], rows, esz);
+        pp.ns[i] = (Ks[i] + pp.kx[i] - 1) / pp.kx[i];
     }
 }
 
-template <typename T, int NT, int XM, int SE>
-static void sk_launch(const Plan *P, int layer, int N, int K, int nks, int smem, cudaStream_t s) {
-    const int nrb = (N + SK_ROWS - 1) / SK_ROWS;
-    k_skinny<T, NT, XM, SE><<<nrb * nks, SK_THREADS, smem, s>>>(P, layer, N, K, nks);
+template <typename T, int OP, int MT>
+static void pg_launch(const Plan *P, const Plan &h, const PdmPlan &pp, int layer, int grid, cudaStream_t s) {
+    const int K = pg_K<OP>(h), kx = pp.kx[OP];
+    for (int k0 = 0; k0 < K; k0 += kx) k_pdm_gemm<T, OP, MT><<<grid, PG_THREADS, PG_SMEM, s>>>(P, layer, k0, kx);
 }
 
-template <typename T, int NT>
-static void pdm_step_nt(const Plan *P, const Plan &h, const SkPlan &sk, cudaStream_t s) {
-    sk_launch<T, NT, XM_FEAT, SE_PROJ>(P, 0, h.d, h.nB * h.d, sk.nks[0], sk.smem, s);
+template <typename T, int MT>
+static void pdm_step_mt(const Plan *P, const Plan &h, const PdmPlan &pp, int grid, cudaStream_t s) {
+    pg_launch<T, OP_PROJ, MT>(P, h, pp, 0, grid, s);
     for (int li = 0; li < h.Ls; ++li) {
-        sk_launch<T, NT, XM_NORM1, SE_QKV>(P, li, h.qkv_rows, h.d, sk.nks[1], sk.smem, s);
+        pg_launch<T, OP_QKV, MT>(P, h, pp, li, grid, s);
+        const int items = (h.Hq + h.Hkv) * (h.hd / 2) + h.kv_rows;
+        k_pdm_rope_kv<T><<<dim3(h.n + 1, (items + 255) / 256), 256, 0, s>>>(P, li);
         launch_pdm_attn<T>(P, h, li, s);
-        sk_launch<T, NT, XM_ATT, SE_OPROJ>(P, li, h.d, h.q_rows, sk.nks[2], sk.smem, s);
-        sk_launch<T, NT, XM_NORM2, SE_GATEUP>(P, li, 2 * h.F, h.d, sk.nks[3], sk.smem, s);
-        sk_launch<T, NT, XM_SILU, SE_DOWN>(P, li, h.d, h.F, sk.nks[4], sk.smem, s);
+        pg_launch<T, OP_OPROJ, MT>(P, h, pp, li, grid, s);
+        pg_launch<T, OP_GATEUP, MT>(P, h, pp, li, grid, s);
+        pg_launch<T, OP_DOWN, MT>(P, h, pp, li, grid, s);
     }
 }
 
 template <typename T>
-void launch_pdm_step(const Plan *P, const Plan &h, const SkPlan &sk, cudaStream_t s) {
-    switch (sk.NT) {
-        case 1: pdm_step_nt<T, 1>(P, h, sk, s); break;
-        case 2: pdm_step_nt<T, 2>(P, h, sk, s); break;
-        case 3: pdm_step_nt<T, 3>(P, h, sk, s); break;
-        default: pdm_step_nt<T, 4>(P, h, sk, s); break;
-    }
+void launch_pdm_step(const Plan *P, const Plan &h, const PdmPlan &pp, int grid, cudaStream_t s) {
+    if (pp.MT == 1) pdm_step_mt<T, 1>(P, h, pp, grid, s);
+    else pdm_step_mt<T, 2>(P, h, pp, grid, s);
 }
 
-template <typename T, int NT>
-static void set_attr_nt(int smem) {
-    cudaFuncSetAttribute(k_skinny<T, NT, XM_FEAT, SE_PROJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(k_skinny<T, NT, XM_NORM1, SE_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(k_skinny<T, NT, XM_ATT, SE_OPROJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(k_skinny<T, NT, XM_NORM2, SE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(k_skinny<T, NT, XM_SILU, SE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <typename T, int MT>
+static void set_attr_mt() {
+    cudaFuncSetAttribute(k_pdm_gemm<T, OP_PROJ, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    cudaFuncSetAttribute(k_pdm_gemm<T, OP_QKV, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    cudaFuncSetAttribute(k_pdm_gemm<T, OP_OPROJ, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    cudaFuncSetAttribute(k_pdm_gemm<T, OP_GATEUP, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    cudaFuncSetAttribute(k_pdm_gemm<T, OP_DOWN, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
 }
 
-void set_pdm_attributes(int smem) {
-    set_attr_nt<float, 1>(smem);
-    set_attr_nt<float, 2>(smem);
-    set_attr_nt<float, 3>(smem);
-    set_attr_nt<float, 4>(smem);
-    set_attr_nt<__nv_bfloat16, 1>(smem);
-    set_attr_nt<__nv_bfloat16, 2>(smem);
-    set_attr_nt<__nv_bfloat16, 3>(smem);
-    set_attr_nt<__nv_bfloat16, 4>(smem);
+void set_pdm_attributes() {
+    set_attr_mt<float, 1>();
+    set_attr_mt<float, 2>();
+    set_attr_mt<__nv_bfloat16, 1>();
+    set_attr_mt<__nv_bfloat16, 2>();
 }
 
-template void launch_pdm_step<float>(const Plan *, const Plan &, const SkPlan &, cudaStream_t);
-template void launch_pdm_step<__nv_bfloat16>(const Plan *, const Plan &, const SkPlan &, cudaStream_t);
+template void launch_pdm_step<float>(const Plan *, const Plan &, const PdmPlan &, int, cudaStream_t);
+template void launch_pdm_step<__nv_bfloat16>(const Plan *, const Plan &, const PdmPlan &, int, cudaStream_t);
 
 }  // namespace spd

@@ -101,6 +101,73 @@ __device__ __noinline__ void c_stage_swiglu(const float *__restrict__ gu, float 
     }
 }
 
+// xs = attention output of stage s: each head's chunk partials (o_c, m_c, l_c) merged in
+// chunk order, x = (sum_c e^{m_c - M} o_c) / (sum_c e^{m_c - M} l_c), M = max_c m_c.
+// wsm: 2 * Hq * nch floats of shared memory.  Ends with a barrier.
+template <typename T>
+__device__ __noinline__ void c_stage_attn(const Plan *__restrict__ P, int s, int pos, float *xs, float *wsm) {
+    const int Hq = P->Hq, hd = P->hd, maxch = P->att_max_chunks, pp = att_part_pitch(hd);
+    const int nch = pos / ATT_CHUNK + 1, tid = threadIdx.x;
+    const float *part = P->att_part + (long long)s * Hq * maxch * pp;
+    float *wl = wsm + Hq * nch;
+    for (int i = tid; i < Hq * nch; i += TG_CONSUMERS) {
+        const int h = i / nch, c = i - h * nch;
+        const float2 ml = *reinterpret_cast<const float2 *>(part + ((long long)h * maxch + c) * pp + hd);
+        wsm[i] = ml.x;
+        wl[i] = ml.y;
+    }
+    named_sync(BAR_C, TG_CONSUMERS);
+    for (int h = tid; h < Hq; h += TG_CONSUMERS) {
+        float M = -INFINITY;
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, wsm[h * nch + c]);
+        float den = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const float w = expf(wsm[h * nch + c] - M);
+            wsm[h * nch + c] = w;
+            den = fmaf(w, wl[h * nch + c], den);
+        }
+        wl[h * nch] = den;
+    }
+    named_sync(BAR_C, TG_CONSUMERS);
+    // 4-element groups, two per thread per pass with up to 8 chunks each in flight
+    const int K = Hq * hd, g4 = K >> 2, q4 = hd >> 2, plane = K >> 1;
+    for (int b = tid; b < g4; b += 2 * TG_CONSUMERS) {
+        for (int c0 = 0; c0 < nch; c0 += 8) {
+            float4 v[2][8];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = b + e * TG_CONSUMERS, h = i / q4, d4 = i - h * q4;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (i < g4 && c0 + u < nch)
+                        v[e][u] = *reinterpret_cast<const float4 *>(part + ((long long)h * maxch + c0 + u) * pp + 4 * d4);
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = b + e * TG_CONSUMERS, h = i / q4;
+                if (i >= g4) continue;
+                float4 *px = reinterpret_cast<float4 *>(xs + xp<T>(4 * i, plane));
+                float4 acc = c0 == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : *px;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (c0 + u < nch) {
+                        const float w = wsm[h * nch + c0 + u];
+                        acc.x = fmaf(w, v[e][u].x, acc.x);
+                        acc.y = fmaf(w, v[e][u].y, acc.y);
+                        acc.z = fmaf(w, v[e][u].z, acc.z);
+                        acc.w = fmaf(w, v[e][u].w, acc.w);
+                    }
+                if (c0 + 8 >= nch) {
+                    const float den = wl[h * nch];
+                    acc = make_float4(acc.x / den, acc.y / den, acc.z / den, acc.w / den);
+                }
+                *px = acc;
+            }
+        }
+    }
+    named_sync(BAR_C, TG_CONSUMERS);
+}
+
 // xs = rms(x) * g over d (x staged first, fixed-order reduction); ends with a barrier
 template <typename T>
 __device__ __noinline__ void c_stage_norm(const float *__restrict__ x, const float *__restrict__ g, int d, float eps, float *xs,
@@ -263,7 +330,9 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
     const int nch = (int)(((long long)K * sizeof(T) + TG_ROWB - 1) / TG_ROWB);
     const int KC = ((K + nch - 1) / nch + VEC - 1) / VEC * VEC;
     // shared memory: x (NRHS x K floats) first, then the ring of 8-row tiles
-    const int xbytes = ((NRHS * K * (int)sizeof(float)) + 127) / 128 * 128;
+    // (the O projection also keeps the attention merge weights, 2 x Hq x chunks floats, after x)
+    const int xfloats = NRHS * K + (EPI == EPI_OPROJ ? 2 * P->Hq * P->att_max_chunks : 0);
+    const int xbytes = (xfloats * (int)sizeof(float) + 127) / 128 * 128;
     const int rowb = (KC * (int)sizeof(T) + 127) / 128 * 128;
     const int stage_bytes = TG_RG * rowb;
     const int NS = min(TG_MAXNS, (TG_SMEM - xbytes) / stage_bytes);
@@ -329,8 +398,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
         if (EPI == EPI_QKV) c_stage_norm<T>(P->X + (long long)slot * d, w.g1, d, P->eps, xs, cred);
         else if (EPI == EPI_GATEUP) c_stage_norm<T>(P->X + (long long)slot * d, w.g2, d, P->eps, xs, cred);
         else if (EPI == EPI_OPROJ) {
-            c_stage_f4<T>(P->ATT + (long long)s * P->q_rows, xs, K);
-            named_sync(BAR_C, TG_CONSUMERS);
+            c_stage_attn<T>(P, s, SL.pos[i], xs, xs + K);
         } else if (EPI == EPI_DOWN) {
             c_stage_swiglu<T>(P->U + (long long)s * 2 * P->F, xs, K);
             named_sync(BAR_C, TG_CONSUMERS);
