@@ -7,7 +7,6 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
-#include <cstdlib>
 #include <string>
 #include <vector>
 
@@ -26,12 +25,11 @@ constexpr int SM_BOUND = 256;       // SM count bound used for workspace sizing
 struct spd_handle {
     Plan h{};
     Plan *dP = nullptr;
-    PdmPlan pp{};
     cudaStream_t s_user = nullptr;                 // caller's stream (may be the legacy default stream)
     cudaStream_t s_main = nullptr, s_pdm = nullptr; // own streams: target rounds, draft module
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_in = nullptr, ev_out = nullptr;
     cudaGraphExec_t g1 = nullptr, gN = nullptr;
-    int grid_gemv = 0, grid_lm = 0, grid_pdm = 0, num_sms = 0;
+    int grid_gemv = 0, grid_lm = 0, num_sms = 0;
     bool prefilled = false;
     std::string err;
     float theta = 1e4f;
@@ -128,7 +126,18 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.QKVp = b.take<float>((size_t)ns * qkv);
     h.ATTp = b.take<float>((size_t)ns * qr);
     h.GUp = b.take<float>((size_t)ns * 2 * d->F);
-    h.ssp = b.take<float>((size_t)SM_BOUND * MAXS);
+    h.ssp = b.take<float>((size_t)MAXS * (d->d / 8));
+    {
+        // draft GEMM K-slab partials: largest slabs x rows x outputs over the five GEMMs
+        int kx[5], nsl[5], MT;
+        pdm_plan(d->d, d->F, qr, c->n_anchors, n, d->dtype, kx, nsl, &MT);
+        const int Ns[5] = {d->d, qkv, d->d, 2 * d->F, d->d};
+        size_t most = 1;
+        for (int i = 0; i < 5; ++i)
+            if (nsl[i] > 1) most = std::max(most, (size_t)nsl[i] * ns * Ns[i]);
+        h.pdm_part = b.take<float>(most);
+        h.pdm_cnt = b.take<int>((size_t)SM_BOUND);
+    }
     h.logits = b.take<float>((size_t)2 * d->V);
     h.dlogits = b.take<float>(c->temperature > 0.f ? (size_t)ns * d->V : 1);
     h.lm_part = b.take<float>((size_t)LM_GRID_MAX * 4);
@@ -169,10 +178,14 @@ template <typename T>
 static void record_step(spd_handle *H, std::vector<int> *pairs) {
     const Plan &h = H->h;
     Plan *P = H->dP;
-    cudaEventRecord(H->ev_fork, H->s_main);
-    cudaStreamWaitEvent(H->s_pdm, H->ev_fork, 0);
-    if (h.Ls > 0) launch_pdm_step<T>(P, h, H->pp, H->grid_pdm, H->s_pdm);
-    cudaEventRecord(H->ev_join, H->s_pdm);
+    // draft module on the second stream, concurrent with the target's rounds
+    const bool separate = h.Ls > 0;
+    if (separate) {
+        cudaEventRecord(H->ev_fork, H->s_main);
+        cudaStreamWaitEvent(H->s_pdm, H->ev_fork, 0);
+        launch_pdm_step<T>(P, h, H->num_sms, H->s_pdm);
+        cudaEventRecord(H->ev_join, H->s_pdm);
+    }
     for (int j = 0; j < h.J; ++j) {
         launch_target_qkv<T>(P, h, j, H->grid_gemv, H->s_main);
         launch_target_attn<T>(P, h, j, H->s_main);
@@ -190,7 +203,7 @@ static void record_step(spd_handle *H, std::vector<int> *pairs) {
         }
         launch_target_down<T>(P, h, j, H->grid_gemv, H->s_main);
     }
-    cudaStreamWaitEvent(H->s_main, H->ev_join, 0);
+    if (separate) cudaStreamWaitEvent(H->s_main, H->ev_join, 0);
     launch_lm_head<T>(P, h, H->grid_lm, H->s_main);
     launch_verify<T>(P, h, H->s_main);
 }
@@ -330,7 +343,7 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
         H->err = "no CUDA device";
         return bail(SPD_ECUDA);
     }
-    pdm_plan(h, H->pp);
+    pdm_plan(h.d, h.F, h.q_rows, h.nB, h.n, h.dtype, h.pdm_kx, h.pdm_ns, &h.pdm_MT);
     const int gsm = gemv_smem_bytes(h);
     set_target_attributes(std::max(gsm, 48 * 1024));
     set_pdm_attributes();
@@ -338,20 +351,6 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
     set_attn_attributes();
     H->num_sms = std::min(H->num_sms, SM_BOUND);
     H->grid_gemv = H->num_sms * target_blocks_per_sm(h.dtype, gemv_smem_bytes(h));
-    // The draft module's GEMMs run on their own stream.  With pdm_sms > 0 they use that many
-    // CTAs (one per SM) and the target's GEMVs the remaining SMs, so both streams stream
-    // weights side by side; with 0 each launch spans the whole GPU and the two take turns.
-    H->grid_pdm = H->num_sms;
-    if (Ls > 0) {
-        int pdm_sms = -1;
-        if (const char *e = std::getenv("SPD_PDM_SMS")) pdm_sms = std::atoi(e);
-        if (pdm_sms < 0) pdm_sms = 0;
-        if (pdm_sms > 0 && pdm_sms < H->num_sms) {
-            H->grid_pdm = pdm_sms;
-            H->grid_gemv = H->num_sms - pdm_sms;
-        }
-    }
-    h.pdm_grid = H->grid_pdm;
     H->grid_lm = std::min(LM_GRID_MAX, H->num_sms * lm_blocks_per_sm(h.dtype, 2 * h.d * 4, h.pdm_lm_head == h.lm_head));
     if (cudaStreamCreateWithFlags(&H->s_main, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&H->s_pdm, cudaStreamNonBlocking) != cudaSuccess ||
@@ -373,6 +372,7 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
     if (cudaMemsetAsync(workspace, 0, (char *)h.kc - (char *)workspace, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.att_cnt, 0, sizeof(int) * MAXS * h.Hkv, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.patt_cnt, 0, sizeof(int) * MAXS * h.Hkv, H->s_main) != cudaSuccess ||
+        cudaMemsetAsync(h.pdm_cnt, 0, sizeof(int) * SM_BOUND, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.lm_cnt, 0, sizeof(int), H->s_main) != cudaSuccess) {
         H->err = "workspace initialisation failed";
         return bail(SPD_ECUDA);

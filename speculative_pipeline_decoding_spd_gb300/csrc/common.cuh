@@ -90,8 +90,11 @@ struct Plan {
     long long pdm_bytes;           // draft module per step (projection + layers)
     long long lm_bytes;            // LM head per step
     float *Xp, *QKVp, *ATTp, *GUp;  // draft module rows: residual, q|k|v, attention, gate|up
-    float *ssp;                    // [pdm_grid][MAXS] per-CTA sums of squares of the Xp rows
-    int pdm_grid;                  // CTAs of every draft GEMM launch
+    float *ssp;                    // [MAXS][d / 8] sums of squares of 8-row groups of the Xp rows
+    float *pdm_part;               // draft GEMM K-slab partials [slab][n+1][N]
+    int *pdm_cnt;                  // draft GEMM row-block arrival counters (zero between launches)
+    int pdm_kx[5], pdm_ns[5];      // draft GEMMs (proj, qkv, o, gate/up, down): K slab width, slabs
+    int pdm_MT;                    // 16-row mma tiles of the draft rows (1: n+1 <= 16, else 2)
     float *logits;                 // [2][V]
     float *dlogits;                // [n+1][V] draft logits per slot (T > 0)
     float *lm_part;                // [grid][2] (val, idx as float bits)
@@ -432,11 +435,9 @@ template <typename T> void launch_target_oproj(const Plan *P, const Plan &h, int
 template <typename T> void launch_target_gateup(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
 template <typename T> void launch_target_down(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s);
 template <typename T> void launch_lm_head(const Plan *P, const Plan &h, int grid, cudaStream_t s);
-// draft GEMMs (proj, qkv, o, gate/up, down): K slab width and slab count; MT = 16-row mma tiles of x
-struct PdmPlan { int kx[5]; int ns[5]; int MT; };
-template <typename T> void launch_pdm_step(const Plan *P, const Plan &h, const PdmPlan &pp, int grid, cudaStream_t s);
+template <typename T> void launch_pdm_step(const Plan *P, const Plan &h, int grid, cudaStream_t s);
 template <typename T> void launch_pdm_attn(const Plan *P, const Plan &h, int layer, cudaStream_t s);
-void pdm_plan(const Plan &h, PdmPlan &pp);
+void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[5], int ns[5], int *MT);
 void set_pdm_attributes();
 void set_target_attributes(int smem);
 void set_prefill_attributes();

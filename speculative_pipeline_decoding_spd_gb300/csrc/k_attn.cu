@@ -15,7 +15,8 @@
 namespace spd {
 
 // Plan-driven launch: problems are the occupied stages with a layer at this round
-// (TARGET) or the draft module's rows (draft layer `arg`).
+// (TARGET, round `arg`) or the draft module's rows at draft layer `arg` (their K,V were
+// appended by the draft QKV epilogue).
 template <typename T, bool TARGET>
 __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const Plan *__restrict__ P, int arg) {
     __shared__ int s_ok, s_pos, s_layer, s_src;
@@ -56,7 +57,6 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const
     a.kc = reinterpret_cast<T *>(TARGET ? P->kc : P->pkc) + kvoff;
     a.vc = reinterpret_cast<T *>(TARGET ? P->vc : P->pvc) + kvoff;
     a.S = s_pos + 1;
-    a.prob = prob;
     a.maxch = P->att_max_chunks;
     a.Hq = P->Hq;
     a.Hkv = Hkv;
@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const
         a.out = P->ATTp + (long long)s_src * P->q_rows;
         a.part = P->patt_part;
         a.cnt = P->patt_cnt;
+        a.prob = s_src;
     }
     attn_cta<T>(a, g, c);
 }

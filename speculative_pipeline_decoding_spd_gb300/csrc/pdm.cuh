@@ -1,0 +1,537 @@
+// Draft-module GEMM, CTA-level device code of the draft kernels (k_pdm.cu).
+//
+// Speculative pipeline decoding, machine review "What carries the argument" / "Core
+// claim": the draft module reads the pipeline's INPUT states, concatenates the target's
+// hidden states at the anchor depths (deeper anchors of in-flight tokens are not yet
+// computed and enter as zeros), projects them to one feature and runs Ls decoder layers.
+// Its rows in one step are the token that left the pipeline last step and the in-flight
+// tokens, at consecutive positions.
+//
+// Every GEMM here multiplies one weight matrix W [N][K] by R <= n+1 row vectors x [R][K]
+// (far more bytes of W than of x: bound by streaming W once from HBM).  A group of CTAs
+// does one GEMM; per CTA:
+//   * a producer warp streams 8-row tiles of W (each row piece up to 6 KB, 1-D bulk
+//     copies) into a shared-memory ring signalled by mbarriers;
+//   * the consumer warps stage the R rows of x for the CTA's K slab in shared memory as bf16
+//     (fp32 for fp32 weights), with the input's RMS normalisation / SiLU product / anchor
+//     masking fused into the staging;
+//   * the 8 consumer warps split each tile's K range into 32-element blocks (block b to
+//     warp b mod 8); per block a warp runs two m16n8k16 tensor-core steps with the x rows
+//     as the 16-row A operand and the 8 weight rows as the B operand, both taking K in the
+//     same permuted order inside the block, so one 16-byte shared-memory read per lane
+//     feeds a whole fragment;
+//   * after the last K piece of a tile group the warps' partial 16x8 products meet in
+//     shared memory and are added in warp order, then the epilogue finishes the outputs.
+// The CTAs of a GEMM split its output rows into row blocks and, when the x rows of all of
+// K do not fit in shared memory, its K range into ns slabs: CTA p works on row block
+// p / ns, slab p % ns.  Slab CTAs leave partial sums; the last to arrive at a row block
+// adds them in slab order and finishes the outputs.
+// Epilogues: the QKV GEMM applies RoPE and appends the rows' K,V to the module's cache
+// (a tile holds 4 rotary pairs: rows i and i + hd/2 of one head, so both halves meet in
+// one warp); projection, O and down finish residual rows and leave per-8-row sums of
+// squares for the next normalisation (independent of how CTAs split the work).
+#pragma once
+
+#include "common.cuh"
+
+namespace spd {
+
+enum { OP_PROJ = 0, OP_QKV, OP_OPROJ, OP_GATEUP, OP_DOWN };
+
+constexpr int PG_CONSUMERS = 256;              // 8 consumer warps
+constexpr int PG_THREADS = PG_CONSUMERS + 32;  // + 1 producer warp
+constexpr int PG_RG = 8;                       // weight rows per tile (the mma's n)
+constexpr int PG_ROWB = 6144;                  // bytes of one row per tile piece, at most
+constexpr int PG_MAXNS = 8;                    // ring stages at most
+constexpr int PG_SMEM = 210 * 1024;            // x + reduction buffers + ring
+constexpr int PG_XMAX = 48 * 1024;             // budget of the x rows of one slab
+constexpr int PG_XRB = 10;                     // register-resident x: 32-element blocks per warp, at most
+constexpr int PG_KB = 32;                      // K elements per warp block
+constexpr int PG_BAR = 1;                      // named barrier of the consumer warps
+
+__host__ __device__ inline int pg_round(int v, int m) { return (v + m - 1) / m * m; }
+// row pitch (bytes) of x and of a weight tile: 128-byte multiple + 64, so the 8 rows that
+// one fragment read touches fall alternately into the two halves of the banks
+__host__ __device__ inline int pg_pitch(int elems, int esz) { return pg_round(elems * esz, 128) + 64; }
+__host__ __device__ inline int pg_xbytes(int rows, int kx, int esz) { return pg_round(rows * pg_pitch(kx, esz), 128); }
+__host__ __device__ inline int pg_redbytes(int MT) { return 2 * (PG_CONSUMERS / 32) * MT * 32 * 16; }
+// K pieces of one slab of kw elements: nch pieces of KC elements (multiples of PG_KB)
+__host__ __device__ inline int pg_nch(int kw, int esz) { return (kw * esz + PG_ROWB - 1) / PG_ROWB; }
+__host__ __device__ inline int pg_kc(int kw, int esz) { return pg_round((kw + pg_nch(kw, esz) - 1) / pg_nch(kw, esz), PG_KB); }
+
+template <int OP> __host__ __device__ inline int pg_N(const Plan &h) {
+    return OP == OP_QKV ? h.qkv_rows : OP == OP_GATEUP ? 2 * h.F : h.d;
+}
+template <int OP> __host__ __device__ inline int pg_K(const Plan &h) {
+    return OP == OP_PROJ ? h.nB * h.d : OP == OP_OPROJ ? h.q_rows : OP == OP_DOWN ? h.F : h.d;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(smem_u32(p)));
+    return r;
+}
+
+// Weight rows of one draft GEMM.  Output row of tile slot q in group g: 8g + q, except for
+// the q and k rows of the QKV GEMM, where group g holds rotary pairs 4g .. 4g+3 (pair u =
+// (head u / (hd/2), element u mod (hd/2))): slots 0..3 the first halves, 4..7 the second.
+template <typename T, int OP>
+struct PgRows {
+    const T *p0, *p1, *p2;
+    int b1, b2, K, hd, qk_groups;
+    __device__ __forceinline__ int row_of(int g, int q) const {
+        if (OP == OP_QKV && g < qk_groups) {
+            const int half = hd >> 1, u = 4 * g + (q & 3), h = u / half;
+            return h * hd + (u - h * half) + (q >= 4 ? half : 0);
+        }
+        return 8 * g + q;
+    }
+    __device__ __forceinline__ const T *ptr(int row) const {
+        if (row < b1) return p0 + (long long)row * K;
+        if (row < b2) return p1 + (long long)(row - b1) * K;
+        return p2 + (long long)(row - b2) * K;
+    }
+};
+template <typename T, int OP>
+__device__ __forceinline__ PgRows<T, OP> pg_rows(const Plan *__restrict__ P, int layer) {
+    PgRows<T, OP> r;
+    r.K = pg_K<OP>(*P);
+    r.hd = P->hd;
+    r.qk_groups = (P->q_rows + P->kv_rows) / 8;
+    r.b1 = r.b2 = 0x7fffffff;
+    r.p1 = r.p2 = nullptr;
+    if (OP == OP_PROJ) {
+        r.p0 = reinterpret_cast<const T *>(P->proj);
+        return r;
+    }
+    const LayerW &w = P->pl[layer];
+    if (OP == OP_QKV) {
+        r.p0 = reinterpret_cast<const T *>(w.wq);
+        r.p1 = reinterpret_cast<const T *>(w.wk);
+        r.p2 = reinterpret_cast<const T *>(w.wv);
+        r.b1 = P->q_rows;
+        r.b2 = P->q_rows + P->kv_rows;
+    } else if (OP == OP_GATEUP) {
+        r.p0 = reinterpret_cast<const T *>(w.wg);
+        r.p1 = reinterpret_cast<const T *>(w.wu);
+        r.b1 = P->F;
+    } else {
+        r.p0 = reinterpret_cast<const T *>(OP == OP_OPROJ ? w.wo : w.wd);
+    }
+    return r;
+}
+
+// ---- x staging (consumer warps only) ---------------------------------------------------
+template <typename XT>
+__device__ __forceinline__ void pg_store4(unsigned char *xs, int pitch, int r, int k, float4 v) {
+    if (sizeof(XT) == 2) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&a);
+        u.y = *reinterpret_cast<uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(xs + r * pitch + k * 2) = u;
+    } else {
+        *reinterpret_cast<float4 *>(xs + r * pitch + k * 4) = v;
+    }
+}
+
+// Per-row RMS statistics of Xp rows 0..R-1 from the per-8-row sums of squares that the GEMM
+// which last finished Xp left in ssp [row][d / 8] (lane-strided, then a fixed shuffle tree).
+static __device__ __noinline__ void pg_row_inv_rms(const Plan *__restrict__ P, int R, float *inv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ng = P->d / 8;
+    for (int r = warp; r < R; r += PG_CONSUMERS / 32) {
+        const float *sp = P->ssp + (long long)r * ng;
+        float s = 0.f;
+        for (int c = lane; c < ng; c += 32) s += sp[c];
+        s = warp_sum(s);
+        if (lane == 0) inv[r] = 1.0f / sqrtf(s / (float)P->d + P->eps);
+    }
+}
+
+// Stage the slab [k0, k0 + kw) of all R rows: items are 4-element groups, 8 in flight per thread.
+template <typename XT, int OP>
+static __device__ __noinline__ void pg_stage_x(const Plan *__restrict__ P, const PdmRows &pr, int layer, int k0, int kw,
+                                               unsigned char *xs, int pitch, const float *inv) {
+    const int R = pr.R, kw4 = kw >> 2, total = R * kw4, d = P->d;
+    const float *g = OP == OP_QKV ? P->pl[layer].g1 : OP == OP_GATEUP ? P->pl[layer].g2 : nullptr;
+    for (int b = threadIdx.x; b < total; b += 8 * PG_CONSUMERS) {
+        float4 v[8], w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * PG_CONSUMERS;
+            if (i >= total) continue;
+            const int r = i / kw4, k = k0 + 4 * (i - r * kw4);
+            if (OP == OP_PROJ) {
+                const int a = k / d, off = k - a * d;
+                v[u] = P->anchors[a] <= pr.depth[r]
+                           ? *reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + a) * d + off)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (OP == OP_QKV || OP == OP_GATEUP) {
+                v[u] = *reinterpret_cast<const float4 *>(P->Xp + (long long)r * d + k);
+                w[u] = *reinterpret_cast<const float4 *>(g + k);
+            } else if (OP == OP_OPROJ) {
+                v[u] = *reinterpret_cast<const float4 *>(P->ATTp + (long long)r * P->q_rows + k);
+            } else {
+                v[u] = *reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + k);
+                w[u] = *reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + P->F + k);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b + u * PG_CONSUMERS;
+            if (i >= total) continue;
+            const int r = i / kw4, kk = 4 * (i - r * kw4);
+            float4 x = v[u];
+            if (OP == OP_QKV || OP == OP_GATEUP) {
+                const float s = inv[r];
+                x = make_float4((x.x * s) * w[u].x, (x.y * s) * w[u].y, (x.z * s) * w[u].z, (x.w * s) * w[u].w);
+            } else if (OP == OP_DOWN) {
+                x = make_float4(silu_f(x.x) * w[u].x, silu_f(x.y) * w[u].y, silu_f(x.z) * w[u].z, silu_f(x.w) * w[u].w);
+            }
+            pg_store4<XT>(xs, pitch, r, kk, x);
+        }
+    }
+}
+
+// Finish output (x row xr, weight row `row`, tile slot wr) of group g with value v.  Called
+// by whole warps of the reduction threads (tid < 128 MT), each thread owning the fixed
+// (xr, wr) pair of the mma fragment layout; `valid` = the pair is a real output.
+template <typename T, int OP>
+__device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmRows &pr, int layer, int g, int xr, int row,
+                                          int wr, float v, bool valid) {
+    if (OP == OP_QKV) {
+        // rotary partner: slot wr ^ 4 of the same x row sits in lane ^ 2 (thread bit 3)
+        const float partner = __shfl_xor_sync(0xffffffffu, v, 8);
+        if (!valid) return;
+        const int pos = pr.pos0 + xr, hd = P->hd, half = hd >> 1;
+        const long long cache = (long long)layer * P->kv_stride + (long long)pos * P->kv_rows;
+        if (row < P->q_rows + P->kv_rows) {
+            const bool first = wr < 4;
+            const int i = row % hd, j = first ? i : i - half;
+            const float2 cs = P->rope[(long long)pos * half + j];
+            const float a = first ? v : partner, b = first ? partner : v;
+            const float y = first ? a * cs.x - b * cs.y : b * cs.x + a * cs.y;
+            if (row < P->q_rows) P->QKVp[(long long)xr * P->qkv_rows + row] = y;
+            else reinterpret_cast<T *>(P->pkc)[cache + (row - P->q_rows)] = WTraits<T>::store(y);
+        } else {
+            reinterpret_cast<T *>(P->pvc)[cache + (row - P->q_rows - P->kv_rows)] = WTraits<T>::store(v);
+        }
+    } else if (OP == OP_GATEUP) {
+        if (valid) P->GUp[(long long)xr * 2 * P->F + row] = v;
+    } else {
+        float o = 0.f;
+        if (valid) {
+            float *dst = P->Xp + (long long)xr * P->d + row;
+            o = OP == OP_PROJ ? v : *dst + v;
+            *dst = o;
+        }
+        // sum of squares of the 8 rows of this group for x row xr (lanes differing in thread
+        // bits 0, 2, 3 hold its 8 weight rows)
+        float sq = o * o;
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 4);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+        if ((threadIdx.x & 13) == 0 && xr < pr.R) P->ssp[(long long)xr * (P->d / 8) + g] = sq;
+    }
+}
+
+// Register-resident x: when one 16-row mma tile covers the rows, the whole K of the GEMM is
+// one piece of a tile and each warp's K blocks are at most PG_XRB, every warp keeps the A
+// fragments of its blocks in registers for the whole launch (the same K blocks meet every
+// tile), and the x rows take no shared memory.
+__host__ __device__ inline bool pg_xreg(int MT, int esz, int K, int ns) {
+    return MT == 1 && esz == 2 && ns == 1 && K * esz <= PG_ROWB && K <= 8 * PG_XRB * PG_KB;
+}
+
+// 8 consecutive x values of row r at GEMM column k (k % 8 == 0), packed as bf16 pairs.
+template <int OP>
+__device__ __forceinline__ uint4 pg_x8(const Plan *__restrict__ P, const PdmRows &pr, int layer, int r, int k,
+                                       const float *inv) {
+    const int d = P->d;
+    float4 a, b;
+    if (OP == OP_PROJ) {
+        const int an = k / d, off = k - an * d;
+        if (P->anchors[an] <= pr.depth[r]) {
+            const float4 *src = reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + an) * d + off);
+            a = src[0];
+            b = src[1];
+        } else {
+            a = b = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    } else if (OP == OP_QKV || OP == OP_GATEUP) {
+        const float *g = OP == OP_QKV ? P->pl[layer].g1 : P->pl[layer].g2;
+        const float4 *src = reinterpret_cast<const float4 *>(P->Xp + (long long)r * d + k);
+        const float4 x0 = src[0], x1 = src[1];
+        const float4 g0 = *reinterpret_cast<const float4 *>(g + k), g1 = *reinterpret_cast<const float4 *>(g + k + 4);
+        const float s = inv[r];
+        a = make_float4((x0.x * s) * g0.x, (x0.y * s) * g0.y, (x0.z * s) * g0.z, (x0.w * s) * g0.w);
+        b = make_float4((x1.x * s) * g1.x, (x1.y * s) * g1.y, (x1.z * s) * g1.z, (x1.w * s) * g1.w);
+    } else if (OP == OP_OPROJ) {
+        const float4 *src = reinterpret_cast<const float4 *>(P->ATTp + (long long)r * P->q_rows + k);
+        a = src[0];
+        b = src[1];
+    } else {
+        const float4 *gs = reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + k);
+        const float4 *us = reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + P->F + k);
+        const float4 g0 = gs[0], g1 = gs[1], u0 = us[0], u1 = us[1];
+        a = make_float4(silu_f(g0.x) * u0.x, silu_f(g0.y) * u0.y, silu_f(g0.z) * u0.z, silu_f(g0.w) * u0.w);
+        b = make_float4(silu_f(g1.x) * u1.x, silu_f(g1.y) * u1.y, silu_f(g1.z) * u1.z, silu_f(g1.w) * u1.w);
+    }
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
+    return make_uint4(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1),
+                      *reinterpret_cast<uint32_t *>(&p2), *reinterpret_cast<uint32_t *>(&p3));
+}
+
+// One CTA's share of a draft GEMM: CTA p of m_pdm (row block p / ns, K slab p % ns).
+// smem: the dynamic shared memory; full/empty: PG_MAXNS mbarriers each, initialised (full
+// count 1, empty count 8) and fenced by the caller; s_inv: MAXS floats.  Called by all
+// PG_THREADS threads (warp 8 is the producer); returns when the CTA's work is done.
+template <typename T, int OP, int MT>
+__device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int layer, int p, int m_pdm,
+                             unsigned char *smem, uint64_t *full, uint64_t *empty, float *s_inv, int *s_flag) {
+    constexpr int ESZ = sizeof(T);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+    const int ns = P->pdm_ns[OP], kx = P->pdm_kx[OP];
+    const int N = pg_N<OP>(*P), K = pg_K<OP>(*P), G8 = N / 8;
+    const int nb = m_pdm / ns, b = p / ns, sl = p - (p / ns) * ns;
+    if (b >= nb || pr.R < 1) return;
+    const int R = pr.R;
+    const int k0 = sl * kx, kw = min(kx, K - k0);
+    const int gb0 = (int)((long long)G8 * b / nb), gb1 = (int)((long long)G8 * (b + 1) / nb);
+    const int nch = pg_nch(kw, ESZ), KC = pg_kc(kw, ESZ);
+    const int xpitch = pg_pitch(kx, ESZ);
+    const int rowb = pg_pitch(KC, ESZ), stage_bytes = PG_RG * rowb;
+    const bool xreg = pg_xreg(MT, ESZ, K, ns);
+    const int xbytes = xreg ? 0 : pg_xbytes(P->n + 1, kx, ESZ);
+    unsigned char *xs = smem;
+    float4 *red = reinterpret_cast<float4 *>(smem + xbytes);
+    unsigned char *stages = smem + xbytes + pg_redbytes(MT);
+    const int NS = min(PG_MAXNS, (PG_SMEM - xbytes - pg_redbytes(MT)) / stage_bytes);
+    const PgRows<T, OP> wrows = pg_rows<T, OP>(P, layer);
+
+    if (warp == PG_CONSUMERS / 32) {
+        // ------------------------------ producer ----------------------------------------
+        if (lane == 0) {
+            uint32_t tile = 0;
+            for (int g = gb0; g < gb1; ++g) {
+                const T *rp[PG_RG];
+#pragma unroll
+                for (int q = 0; q < PG_RG; ++q) rp[q] = wrows.ptr(wrows.row_of(g, q)) + k0;
+                for (int c = 0; c < nch; ++c) {
+                    const int kc0 = c * KC, len = min(KC, kw - kc0);
+                    const int sidx = tile % NS;
+                    const uint32_t u = tile / NS;
+                    if (!mbar_wait(&empty[sidx], (u & 1) ^ 1)) P->st->error = ERR_TIMEOUT;
+                    const uint32_t bytes = (uint32_t)len * ESZ;
+                    mbar_expect_tx(&full[sidx], bytes * PG_RG);
+#pragma unroll
+                    for (int q = 0; q < PG_RG; ++q) bulk_g2s(stages + sidx * stage_bytes + q * rowb, rp[q] + kc0, bytes, &full[sidx]);
+                    ++tile;
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------ consumers -------------------------------------------
+    if (OP == OP_QKV || OP == OP_GATEUP) {
+        pg_row_inv_rms(P, R, s_inv);
+        named_sync(PG_BAR, PG_CONSUMERS);
+    }
+    // register-resident x (bf16, one mma tile): lane (gq, tq) of warp w holds rows gq and gq + 8,
+    // elements 8tq..8tq+7 of blocks w, w + 8, ... of the GEMM's K
+    uint4 xf[PG_XRB][2];
+    if constexpr (ESZ == 2 && MT == 1) {
+        if (xreg) {
+            const int gq = lane >> 2, tq = lane & 3, nblk = kw / PG_KB;
+#pragma unroll
+            for (int j = 0; j < PG_XRB; ++j) {
+                const int bb = warp + 8 * j, k = k0 + bb * PG_KB + 8 * tq;
+                xf[j][0] = bb < nblk && gq < R ? pg_x8<OP>(P, pr, layer, gq, k, s_inv) : make_uint4(0u, 0u, 0u, 0u);
+                xf[j][1] = bb < nblk && gq + 8 < R ? pg_x8<OP>(P, pr, layer, gq + 8, k, s_inv) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
+    if (!xreg) {
+        pg_stage_x<T, OP>(P, pr, layer, k0, kw, xs, xpitch, s_inv);
+        named_sync(PG_BAR, PG_CONSUMERS);
+    }
+
+    // reduction thread t (< 128 MT) owns x row xr_t and tile slot wr_t of every group
+    const int rm = tid >> 7, rl = (tid >> 2) & 31, rreg = tid & 3;
+    const int xr_t = rm * 16 + (rreg >> 1) * 8 + (rl >> 2), wr_t = (rl & 3) * 2 + (rreg & 1);
+    float *part = P->pdm_part;   // [ns][n+1][N] slab partials
+    const int gq = lane >> 2, tq = lane & 3;
+    uint32_t tile = 0;
+    int buf = 0;
+    for (int g = gb0; g < gb1; ++g) {
+        // bf16: acc[4m..4m+3] is the m-th 16x8 mma accumulator fragment; fp32: acc[j] is the
+        // (x row (lane >> 3) + 4j, tile slot lane & 7) product
+        float acc[4 * MT];
+#pragma unroll
+        for (int j = 0; j < 4 * MT; ++j) acc[j] = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const int kc0 = c * KC, len = min(KC, kw - kc0), nblk = len / PG_KB;
+            const int sidx = tile % NS;
+            const uint32_t u = tile / NS;
+            if (!mbar_wait(&full[sidx], u & 1)) P->st->error = ERR_TIMEOUT;
+            const unsigned char *tb = stages + sidx * stage_bytes;
+            bool done_xreg = false;
+            if constexpr (ESZ == 2 && MT == 1) {
+                if (xreg) {
+                    // one piece per tile (nch == 1): block bb = warp + 8j uses the j-th registers
+                    const unsigned char *wp = tb + gq * rowb + tq * 16;
+                    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+                    float(&f)[4] = *reinterpret_cast<float(*)[4]>(&acc[0]);
+#pragma unroll
+                    for (int j = 0; j < PG_XRB; ++j) {
+                        const int bb = warp + 8 * j;
+                        if (bb < nblk) {
+                            const uint4 w = lds128(wp + bb * 64);
+                            mma_bf16(f, xf[j][0].x, xf[j][1].x, xf[j][0].y, xf[j][1].y, w.x, w.y);
+                            mma_bf16(acc2, xf[j][0].z, xf[j][1].z, xf[j][0].w, xf[j][1].w, w.z, w.w);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[j] += acc2[j];
+                    done_xreg = true;
+                }
+            }
+            if (done_xreg) {
+            } else if constexpr (ESZ == 2) {
+                // lane (gq, tq): tile slot gq, x rows gq and gq + 8 (+16 m), elements 8tq..8tq+7 of
+                // each 32-block; the two mma steps take elements {8tq..8tq+3} and {8tq+4..8tq+7}
+                // and go to two accumulator chains (added at the end of the piece)
+                const unsigned char *wp = tb + gq * rowb + tq * 16;
+                const unsigned char *xp = xs + gq * xpitch + kc0 * 2 + tq * 16;
+                bool xv[MT][2];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    xv[m][0] = m * 16 + gq < R;
+                    xv[m][1] = m * 16 + 8 + gq < R;
+                }
+                float acc2[4 * MT];
+#pragma unroll
+                for (int j = 0; j < 4 * MT; ++j) acc2[j] = 0.f;
+                for (int bb = warp; bb < nblk; bb += PG_CONSUMERS / 32) {
+                    const uint4 w = lds128(wp + bb * 64);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 xa = xv[m][0] ? lds128(xp + (m * 16) * xpitch + bb * 64) : z;
+                        const uint4 xb = xv[m][1] ? lds128(xp + (m * 16 + 8) * xpitch + bb * 64) : z;
+                        float(&f)[4] = *reinterpret_cast<float(*)[4]>(&acc[4 * m]);
+                        float(&f2)[4] = *reinterpret_cast<float(*)[4]>(&acc2[4 * m]);
+                        mma_bf16(f, xa.x, xb.x, xa.y, xb.y, w.x, w.y);
+                        mma_bf16(f2, xa.z, xb.z, xa.w, xb.w, w.z, w.w);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4 * MT; ++j) acc[j] += acc2[j];
+            } else {
+                // fp32 weights: plain FMAs in element order
+                const int wrow = lane & 7, xq = lane >> 3;
+                const float *wp = reinterpret_cast<const float *>(tb + wrow * rowb);
+                for (int bb = warp; bb < nblk; bb += PG_CONSUMERS / 32) {
+                    for (int e = 0; e < PG_KB; ++e) {
+                        const int k = bb * PG_KB + e;
+                        const float wv = wp[k];
+#pragma unroll
+                        for (int j = 0; j < 4 * MT; ++j) {
+                            const int xr = xq + 4 * j;
+                            if (xr < R) acc[j] = fmaf(wv, reinterpret_cast<const float *>(xs + xr * xpitch)[kc0 + k], acc[j]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sidx]);
+            ++tile;
+        }
+        // ---- partial products of all warps in the fragment layout [buf][warp][m][lane] x 4:
+        // float (m, lane, reg) = (x row 16m + 8(reg >> 1) + lane / 4, slot 2(lane % 4) + reg % 2)
+        if constexpr (ESZ == 2) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                red[((buf * (PG_CONSUMERS / 32) + warp) * MT + m) * 32 + lane] =
+                    make_float4(acc[4 * m], acc[4 * m + 1], acc[4 * m + 2], acc[4 * m + 3]);
+        } else {
+            float *rf = reinterpret_cast<float *>(red);
+            const int wrow = lane & 7, xq = lane >> 3;
+#pragma unroll
+            for (int j = 0; j < 4 * MT; ++j) {
+                const int xr = xq + 4 * j, m = xr >> 4, r16 = xr & 15;
+                const int l2 = (r16 & 7) * 4 + (wrow >> 1), reg = (r16 >> 3) * 2 + (wrow & 1);
+                rf[(((buf * (PG_CONSUMERS / 32) + warp) * MT + m) * 32 + l2) * 4 + reg] = acc[j];
+            }
+        }
+        named_sync(PG_BAR, PG_CONSUMERS);
+        if (tid < 128 * MT) {
+            const float *rf = reinterpret_cast<const float *>(red);
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < PG_CONSUMERS / 32; ++w) s += rf[(((buf * (PG_CONSUMERS / 32) + w) * MT + rm) * 32 + rl) * 4 + rreg];
+            const int row = wrows.row_of(g, wr_t);
+            if (ns == 1) pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R);
+            else if (xr_t < R) part[((long long)sl * (P->n + 1) + xr_t) * N + row] = s;
+        }
+        buf ^= 1;
+    }
+    if (ns == 1) return;
+
+    // ---- K slabs: the last CTA of the row block adds the slab partials in slab order
+    __threadfence();
+    named_sync(PG_BAR, PG_CONSUMERS);
+    if (tid == 0) *s_flag = atomicAdd(P->pdm_cnt + b, 1) == ns - 1;
+    named_sync(PG_BAR, PG_CONSUMERS);
+    if (!*s_flag) return;
+    __threadfence();
+    // all consumer threads: 256 / (128 MT) groups per pass, PG_FIN passes' slab loads in flight
+    // together; thread t keeps the fixed (x row, slot) pair of the fragment layout
+    {
+        constexpr int GPP = 2 / MT;          // groups per pass
+        constexpr int PG_FIN = 4;            // passes per batch
+        const int gsub = tid / (128 * MT), t = tid - gsub * (128 * MT);
+        const int xr = (t >> 7) * 16 + ((t & 3) >> 1) * 8 + ((t >> 2) & 31) / 4, wr = (((t >> 2) & 31) & 3) * 2 + (t & 1);
+        for (int g0 = gb0; g0 < gb1; g0 += GPP * PG_FIN) {
+            float sum[PG_FIN];
+#pragma unroll
+            for (int f = 0; f < PG_FIN; ++f) sum[f] = 0.f;
+            for (int s0 = 0; s0 < ns; s0 += 4) {
+                float v[PG_FIN][4];
+#pragma unroll
+                for (int f = 0; f < PG_FIN; ++f) {
+                    const int g = g0 + f * GPP + gsub;
+                    const int row = wrows.row_of(min(g, gb1 - 1), wr);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        v[f][q] = (g < gb1 && xr < R && s0 + q < ns)
+                                      ? __ldcg(part + ((long long)(s0 + q) * (P->n + 1) + xr) * N + row) : 0.f;
+                }
+#pragma unroll
+                for (int f = 0; f < PG_FIN; ++f)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (s0 + q < ns) sum[f] += v[f][q];
+            }
+#pragma unroll
+            for (int f = 0; f < PG_FIN; ++f) {
+                const int g = g0 + f * GPP + gsub;
+                // warp-uniform: the 32 threads of a warp share gsub, hence g
+                if (g < gb1) pg_finish<T, OP>(P, pr, layer, g, xr, wrows.row_of(g, wr), wr, sum[f], xr < R);
+            }
+        }
+    }
+    if (tid == 0) P->pdm_cnt[b] = 0;
+}
+
+}  // namespace spd

@@ -33,7 +33,7 @@ class Engine:
     def __init__(self, dims, target: Dict, pdm: Optional[Dict], n: int, anchors: Sequence[int], *,
                  max_seq: int, max_new: int, temperature: float = 0.0, seed: int = 2, force_p: float = -1.0,
                  forced_ref: Optional[torch.Tensor] = None, graph: bool = True, timing: bool = False,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None, workspace_fill: Optional[int] = None):
         self.dims = dims
         self.n = n
         self.max_new = max_new
@@ -60,6 +60,8 @@ class Engine:
                                 int(forced_ref.numel()) if forced_ref is not None else 0, int(graph), int(timing))
         self.ws_bytes = B.spd_workspace_bytes(self.cd, self.pw, self.cfg)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        if workspace_fill is not None:   # tests: the library must not rely on zeroed memory
+            self.workspace.fill_(workspace_fill)
         self.stream = stream if stream is not None else torch.cuda.current_stream()
         self.h = B.spd_create(self.cd, self.tw, self.pw, self.cfg, self.workspace.data_ptr(), self.ws_bytes,
                               self.stream.cuda_stream)

@@ -25,6 +25,11 @@ HD128 = Case(si.ModelDims(L=5, d=512, Hq=8, Hkv=2, hd=128, F=1024, V=3000), n=4,
 # bf16, rows longer than one 4 KB tile chunk (d 2560, F 2304: two K chunks per row)
 MULTI = Case(si.ModelDims(L=4, d=2560, Hq=8, Hkv=2, hd=128, F=2304, V=1000), n=3, anchors=(0, 2, 4), Ls=1,
              prompt_len=200, max_new=40, norms="perturbed")
+# bf16, 16 stages of 2 layers: 17 draft rows take two 16-row mma tiles
+WIDE = Case(si.ModelDims(L=32, d=256, Hq=4, Hkv=2, hd=64, F=512, V=1500), n=16, anchors=(0, 16, 32), Ls=1,
+            prompt_len=40, max_new=40, norms="perturbed")
+# MULTI's draft projection (K = 5 x 2560) is split into K slabs across CTAs; its QKV, O, gate/up
+# and down keep x in registers (one 16-row tile, K <= 2560); WIDE's 17 rows keep x in shared memory.
 
 
 def _prefill_logits_close(case, pf):
@@ -44,7 +49,7 @@ def test_prefill_logits(case):
     _prefill_logits_close(case, pf)
 
 
-@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI], ids=["tiny", "small", "hd128", "multi"])
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI, WIDE], ids=["tiny", "small", "hd128", "multi", "wide"])
 def test_greedy_draft_module_replay(case):
     toks, tr, st, pf = run_gpu(case)
     o, rep = replay_oracle(case, tr, toks)
@@ -53,8 +58,8 @@ def test_greedy_draft_module_replay(case):
     assert st["N"] == case.max_new - 1 and st["K"] == len(tr)
 
 
-@pytest.mark.parametrize("case,p", [(TINY, 0.6), (SMALL, 0.5), (SMALL, 0.9), (HD128, 0.7), (MULTI, 0.6)],
-                         ids=["tiny-0.6", "small-0.5", "small-0.9", "hd128-0.7", "multi-0.6"])
+@pytest.mark.parametrize("case,p", [(TINY, 0.6), (SMALL, 0.5), (SMALL, 0.9), (HD128, 0.7), (MULTI, 0.6), (WIDE, 0.8)],
+                         ids=["tiny-0.6", "small-0.5", "small-0.9", "hd128-0.7", "multi-0.6", "wide-0.8"])
 def test_forced_draft_replay(case, p):
     ar = ar_reference(case)
     tg, pd, prompt, m, _, _ = materialise(case)
@@ -80,6 +85,16 @@ def test_pipeline_equals_single_stage_bitwise(case):
         for r in tr:
             if r["exit_pos"] >= 0:
                 assert r["target_logit"] == ar_logit[r["exit_pos"]], (n, r["exit_pos"])
+
+
+@pytest.mark.parametrize("case,n", [(MULTI, 1), (MULTI, 3), (SMALL, 3)], ids=["multi-1", "multi-3", "small-3"])
+def test_workspace_contents_do_not_matter(case, n):
+    """The workspace the caller hands over holds garbage (here all bytes 0xFF): every counter
+    and state word the library uses must be initialised by spd_create / spd_prefill."""
+    a = run_gpu(case, n=n)[:2]
+    b = run_gpu(case, n=n, workspace_fill=0xFF)[:2]
+    assert a[0] == b[0]
+    assert [r["len"] for r in a[1]] == [r["len"] for r in b[1]]
 
 
 def test_graph_and_eager_agree():
