@@ -334,6 +334,38 @@ class SPDOracle:
         self.trace.append(rec)
         return rec
 
+    def fork(self, n: Optional[int] = None, forced_p: Optional[float] = None,
+             forced_ref: Optional[Sequence[int]] = None, replay: Optional[Replay] = None) -> "SPDOracle":
+        """A copy of this simulator right after its prefill, before the first step, with its
+        own stage count, draft rule and replay record: several runs from one prompt pass.
+        The model's weights are shared; caches, token list and stage slots are copied."""
+        if self.t != 0 or self.K != 0 or not self.tokens:
+            raise ValueError("fork only between prefill and the first step")
+        if isinstance(self.kv, TrackedCache):
+            raise ValueError("fork does not carry schedule tracking")
+        if forced_p is not None and forced_ref is None:
+            raise ValueError("forced drafts need the reference stream")
+        o = SPDOracle.__new__(SPDOracle)
+        o.__dict__.update(self.__dict__)
+        o.n = self.n if n is None else n
+        o.b = stage_bounds(self.m.dm.L, o.n)
+        o.forced_p, o.ref = forced_p, (None if forced_ref is None else np.asarray(forced_ref))
+        o.replay = replay
+        for name in ("kv", "pkv"):
+            src = getattr(self, name)
+            c = KVCache.__new__(KVCache)
+            c.K = [k.copy() for k in src.K]
+            c.V = [v.copy() for v in src.V]
+            c.length = list(src.length)
+            setattr(o, name, c)
+        o.tokens = list(self.tokens)
+        y0 = self.slots[0]
+        o.slots = [_Tok(y0.pos, y0.tok, y0.H.copy(), {a: h.copy() for a, h in y0.anchors.items()}, y0.pD)]
+        o.slots += [None] * (o.n - 1)
+        o.pending = None
+        o.trace = []
+        return o
+
     def run(self, prompt: Sequence[int], max_new: int, max_steps: Optional[int] = None) -> List[int]:
         self.prefill(prompt)
         Sp = len(prompt)

@@ -38,6 +38,13 @@ class Case:
     def tol(self):
         return 1e-4 if self.dm.dtype == "fp32" else 2e-2
 
+    @property
+    def tol_draft(self):
+        """Draft-module logits: at bf16 its GEMMs take bf16 activations (tensor-core operands)
+        on top of full-depth target states that already carry the target's rounding, so the
+        bound is twice the target's; at fp32 the module computes in fp32 like the target."""
+        return self.tol if self.dm.dtype == "fp32" else 2 * self.tol
+
 
 _cache = {}
 
@@ -97,18 +104,21 @@ def replay_oracle(case: Case, gpu_trace, gpu_tokens, n: Optional[int] = None, to
 def compare(case: Case, gpu_trace, o: SPDOracle, rep: Replay, check_logits=True):
     """Exact agreement of the integer trace; logits within the case tolerance."""
     assert rep.mismatches == [], rep.mismatches[:5]
-    worst = 0.0
+    worst, where, worst_d, where_d = 0.0, None, 0.0, None
     for g, r in zip(gpu_trace, o.trace):
         for k in ("exit_pos", "accept", "commit", "draft", "new_draft", "len", "N"):
             assert g[k] == r[k], (k, g["t"], g[k], r[k])
         if check_logits and r["target_logit"] is not None:
             err = abs(g["target_logit"] - r["target_logit"]) / max(1.0, abs(r["target_logit"]))
-            worst = max(worst, err)
+            if err > worst:
+                worst, where = err, (g["t"], g["target_logit"], r["target_logit"])
         if check_logits and r["pdm_logit"] is not None and r["pdm_top"] == g["pdm_top"]:
             err = abs(g["pdm_logit"] - r["pdm_logit"]) / max(1.0, abs(r["pdm_logit"]))
-            worst = max(worst, err)
-    assert worst <= case.tol, worst
-    return worst
+            if err > worst_d:
+                worst_d, where_d = err, (g["t"], g["pdm_logit"], r["pdm_logit"])
+    assert worst <= case.tol, ("target logit", worst, where)
+    assert worst_d <= case.tol_draft, ("draft logit", worst_d, where_d)
+    return max(worst, worst_d)
 
 
 def ar_reference(case: Case):

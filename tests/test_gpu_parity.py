@@ -28,6 +28,10 @@ MULTI = Case(si.ModelDims(L=4, d=2560, Hq=8, Hkv=2, hd=128, F=2304, V=1000), n=3
 # bf16, 16 stages of 2 layers: 17 draft rows take two 16-row mma tiles
 WIDE = Case(si.ModelDims(L=32, d=256, Hq=4, Hkv=2, hd=64, F=512, V=1500), n=16, anchors=(0, 16, 32), Ls=1,
             prompt_len=40, max_new=40, norms="perturbed")
+# bf16, d 2560 with 17 draft rows: the draft QKV and gate/up need two K slabs (RoPE and KV append
+# happen in the slab-finishing pass), down three
+WIDEK = Case(si.ModelDims(L=32, d=2560, Hq=8, Hkv=2, hd=128, F=2560, V=1000), n=16, anchors=(0, 16, 32), Ls=1,
+             prompt_len=40, max_new=40, norms="perturbed")
 # MULTI's draft projection (K = 5 x 2560) is split into K slabs across CTAs; its QKV, O, gate/up
 # and down keep x in registers (one 16-row tile, K <= 2560); WIDE's 17 rows keep x in shared memory.
 
@@ -49,7 +53,7 @@ def test_prefill_logits(case):
     _prefill_logits_close(case, pf)
 
 
-@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI, WIDE], ids=["tiny", "small", "hd128", "multi", "wide"])
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI, WIDE, WIDEK], ids=["tiny", "small", "hd128", "multi", "wide", "widek"])
 def test_greedy_draft_module_replay(case):
     toks, tr, st, pf = run_gpu(case)
     o, rep = replay_oracle(case, tr, toks)

@@ -197,3 +197,29 @@ def test_replay_decisions_reproduces_simulator_trace():
     got = replay_decisions(3, m.dm.L, len(prompt), o.trace)
     for g, r in zip(got, o.trace):
         assert (g["exit_pos"], g["accept"], g["commit"], g["len"]) == (r["exit_pos"], r["accept"], r["commit"], r["len"])
+
+
+def test_fork_after_prefill_equals_fresh_runs():
+    """A fork taken right after one prefill runs exactly like a fresh simulator that did its
+    own prefill: for other stage counts and draft rules, and without disturbing the parent."""
+    m = micro_model(seed=2)
+    prompt = si.make_prompt(m.dm.V, 6, seed=4)
+    ar = ar_decode(m, prompt, 18, 72)
+    ref = list(prompt) + ar + [0] * 8
+    base = SPDOracle(m, 3, 72, seed=9)
+    base.prefill(prompt)
+    for n, p in [(3, None), (2, 0.5), (4, 0.8), (1, 0.3)]:
+        kw = dict(forced_p=p, forced_ref=ref) if p is not None else {}
+        f = base.fork(n=n, **kw)
+        fresh = SPDOracle(m, n, 72, seed=9, **kw)
+        fresh.prefill(prompt)
+        for _ in range(14):
+            assert f.step() == fresh.step()
+        assert f.tokens == fresh.tokens
+    # the parent is untouched and still runs like a fresh one
+    fresh = SPDOracle(m, 3, 72, seed=9)
+    fresh.prefill(prompt)
+    for _ in range(10):
+        assert base.step() == fresh.step()
+    with pytest.raises(ValueError):
+        base.fork()
