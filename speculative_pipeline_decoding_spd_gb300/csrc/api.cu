@@ -344,6 +344,7 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
         return bail(SPD_ECUDA);
     }
     pdm_plan(h.d, h.F, h.q_rows, h.nB, h.n, h.dtype, h.pdm_kx, h.pdm_ns, &h.pdm_MT);
+    h.pdl = 1;
     const int gsm = gemv_smem_bytes(h);
     set_target_attributes(std::max(gsm, 48 * 1024));
     set_pdm_attributes();

@@ -110,6 +110,10 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
             cp_async16(Vs + j * KP + 4 * q, vb + off);
         }
     }
+    // ---- the chunk's older positions come from earlier steps; q, k_new and v_new from the
+    // preceding launch of this stream
+    pdl_wait();
+    pdl_trigger();
     // ---- q (rotated here when raw), k_new / v_new appended by the chunk owner
     if (a.rope) {
         for (int idx = tid; idx < G * half; idx += ATT_THREADS) {

@@ -95,6 +95,7 @@ struct Plan {
     int *pdm_cnt;                  // draft GEMM row-block arrival counters (zero between launches)
     int pdm_kx[5], pdm_ns[5];      // draft GEMMs (proj, qkv, o, gate/up, down): K slab width, slabs
     int pdm_MT;                    // 16-row mma tiles of the draft rows (1: n+1 <= 16, else 2)
+    int pdl;                       // step kernels launched with programmatic dependent launch
     float *logits;                 // [2][V]
     float *dlogits;                // [n+1][V] draft logits per slot (T > 0)
     float *lm_part;                // [grid][2] (val, idx as float bits)
@@ -157,6 +158,16 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Programmatic dependent launch.  Step kernels are launched so that the next kernel of the
+// stream may start while this one drains: pdl_wait() blocks until the preceding kernel has
+// completed and its writes are visible (a no-op when it was launched without the attribute);
+// pdl_trigger() lets the following kernel start once every CTA of this one has triggered or
+// exited.  Each kernel triggers only after its own wait, so when a kernel starts, every
+// kernel before its predecessor has completed: before its wait it may read weights and the
+// step-stable slot state, nothing its predecessor writes, and it writes nothing global.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Barrier among the first `threads` threads of the CTA (id 0 is __syncthreads').
 __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -424,6 +435,23 @@ __device__ __forceinline__ void warp_pdm_rows(const Plan *__restrict__ P, PdmRow
         if (done) *done = st->done;
     }
     __syncwarp();
+}
+
+// Launch with (pdl = true) or without the programmatic-serialisation attribute.
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                   Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // ---------------------------------------------------------------------------------

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const
     }
     __syncthreads();
     if (!s_ok) return;
+    if (!TARGET) pdl_wait();   // the rows' K,V were appended by the preceding draft QKV launch
     AttnArgs<T> a;
     const long long kvoff = (long long)s_layer * P->kv_stride;
     a.kc = reinterpret_cast<T *>(TARGET ? P->kc : P->pkc) + kvoff;
@@ -109,12 +110,12 @@ void set_attn_attributes() {
 template <typename T>
 void launch_target_attn(const Plan *P, const Plan &h, int round, cudaStream_t s) {
     dim3 grid(h.att_max_chunks * h.Hkv, h.n);
-    k_attn<T, true><<<grid, ATT_THREADS, att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s>>>(P, round);
+    launch_k(k_attn<T, true>, grid, dim3(ATT_THREADS), att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s, h.pdl != 0, P, round);
 }
 template <typename T>
 void launch_pdm_attn(const Plan *P, const Plan &h, int layer, cudaStream_t s) {
     dim3 grid(h.att_max_chunks * h.Hkv, h.n + 1);
-    k_attn<T, false><<<grid, ATT_THREADS, att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s>>>(P, layer);
+    launch_k(k_attn<T, false>, grid, dim3(ATT_THREADS), att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s, h.pdl != 0, P, layer);
 }
 
 template void launch_target_attn<float>(const Plan *, const Plan &, int, cudaStream_t);

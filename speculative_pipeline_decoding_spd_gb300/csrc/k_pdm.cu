@@ -53,19 +53,21 @@ void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[5], int
 }
 
 template <typename T, int OP, int MT>
-static void pg_launch(const Plan *P, int layer, int grid, cudaStream_t s) {
-    k_pdm_gemm<T, OP, MT><<<grid, PG_THREADS, PG_SMEM, s>>>(P, layer);
+static void pg_launch(const Plan *P, const Plan &h, int layer, int grid, cudaStream_t s) {
+    // the projection opens the draft stream's step (it follows the fork from the target's
+    // stream): a full dependency; the rest may start while their predecessor drains
+    launch_k(k_pdm_gemm<T, OP, MT>, dim3(grid), dim3(PG_THREADS), PG_SMEM, s, h.pdl != 0 && OP != OP_PROJ, P, layer);
 }
 
 template <typename T, int MT>
 static void pdm_step_mt(const Plan *P, const Plan &h, int grid, cudaStream_t s) {
-    pg_launch<T, OP_PROJ, MT>(P, 0, grid, s);
+    pg_launch<T, OP_PROJ, MT>(P, h, 0, grid, s);
     for (int li = 0; li < h.Ls; ++li) {
-        pg_launch<T, OP_QKV, MT>(P, li, grid, s);
+        pg_launch<T, OP_QKV, MT>(P, h, li, grid, s);
         launch_pdm_attn<T>(P, h, li, s);
-        pg_launch<T, OP_OPROJ, MT>(P, li, grid, s);
-        pg_launch<T, OP_GATEUP, MT>(P, li, grid, s);
-        pg_launch<T, OP_DOWN, MT>(P, li, grid, s);
+        pg_launch<T, OP_OPROJ, MT>(P, h, li, grid, s);
+        pg_launch<T, OP_GATEUP, MT>(P, h, li, grid, s);
+        pg_launch<T, OP_DOWN, MT>(P, h, li, grid, s);
     }
 }
 

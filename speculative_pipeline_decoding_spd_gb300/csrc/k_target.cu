@@ -297,6 +297,14 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
     __shared__ int s_bi[2][TG_CONSUMERS / 32];
     const DevState *st = P->st;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the first launch of a step follows verification, which rewrites the slot state: it
+    // waits before reading it; every later launch of the step reads the (stable) state and
+    // starts streaming weights before its predecessor has finished
+    const bool wait_first = EPI == EPI_QKV && round == 0;
+    if (wait_first) {
+        pdl_wait();
+        pdl_trigger();
+    }
     if (warp == 0) {
         if (EPI == EPI_LM) {
             // exit slot (stage n-1 occupied?) and the draft module's newest row
@@ -380,6 +388,10 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
     }
 
     // ------------------------------ consumers -----------------------------------------
+    if (!wait_first) {
+        pdl_wait();   // the inputs staged below come from the preceding launch
+        pdl_trigger();
+    }
     const int tid = threadIdx.x;
     float bv[2] = {-INFINITY, -INFINITY};
     int bi[2] = {0x7fffffff, 0x7fffffff};
@@ -571,7 +583,7 @@ static int smem_for(const Plan &, int) { return TG_SMEM; }
 
 template <typename T, int EPI>
 static void launch_epi(const Plan *P, const Plan &h, int round, int grid, cudaStream_t s) {
-    k_gemv<T, EPI, true><<<grid, TG_THREADS, smem_for(h, EPI), s>>>(P, round);
+    launch_k(k_gemv<T, EPI, true>, dim3(grid), dim3(TG_THREADS), smem_for(h, EPI), s, h.pdl != 0, P, round);
 }
 
 template <typename T>
@@ -593,9 +605,9 @@ void launch_target_down(const Plan *P, const Plan &h, int round, int grid, cudaS
 template <typename T>
 void launch_lm_head(const Plan *P, const Plan &h, int grid, cudaStream_t s) {
     if (h.pdm_lm_head == h.lm_head)
-        k_gemv<T, EPI_LM, true><<<grid, TG_THREADS, smem_for(h, EPI_LM), s>>>(P, 0);
+        launch_k(k_gemv<T, EPI_LM, true>, dim3(grid), dim3(TG_THREADS), smem_for(h, EPI_LM), s, h.pdl != 0, P, 0);
     else
-        k_gemv<T, EPI_LM, false><<<grid, TG_THREADS, smem_for(h, EPI_LM), s>>>(P, 0);
+        launch_k(k_gemv<T, EPI_LM, false>, dim3(grid), dim3(TG_THREADS), smem_for(h, EPI_LM), s, h.pdl != 0, P, 0);
 }
 
 int gemv_smem_bytes(const Plan &h) {

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
     DevState *st = P->st;
     const int n = P->n, ns = n + 1, V = P->V;
     const float T_ = P->temperature;
+    pdl_wait();   // logits and argmax of the LM head launch
+    pdl_trigger();
     if (threadIdx.x == 0) {
         s_done = st->done;
         if (!s_done) {
@@ -371,7 +373,7 @@ __global__ void __launch_bounds__(VT) k_prefill_finalize(const Plan *__restrict_
 
 template <typename T>
 void launch_verify(const Plan *P, const Plan &h, cudaStream_t s) {
-    k_verify<T><<<1, VT, 0, s>>>(P);
+    launch_k(k_verify<T>, dim3(1), dim3(VT), 0, s, h.pdl != 0, P);
 }
 template <typename T>
 void launch_prefill_finalize(const Plan *P, int prompt_len, cudaStream_t s) {

@@ -343,6 +343,8 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     }
 
     // ------------------------------ consumers -------------------------------------------
+    pdl_wait();   // x, its statistics and the counters belong to the preceding launch
+    pdl_trigger();
     if (OP == OP_QKV || OP == OP_GATEUP) {
         pg_row_inv_rms(P, R, s_inv);
         named_sync(PG_BAR, PG_CONSUMERS);
