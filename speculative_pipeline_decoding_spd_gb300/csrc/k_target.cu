@@ -230,6 +230,40 @@ __device__ __forceinline__ float dot_x<__nv_bfloat16>(const uint4 &w, const floa
     return acc;
 }
 
+// x values that one 16-byte weight vector at element e meets, loaded once and applied to
+// several weight rows (the LM head's paired tiles).
+template <typename T> struct XV;
+template <> struct XV<float> {
+    float4 a;
+    __device__ __forceinline__ void load(const float *x, int e, int) { a = *reinterpret_cast<const float4 *>(x + e); }
+    __device__ __forceinline__ float dot(const uint4 &w, float acc) const {
+        acc = fmaf(__uint_as_float(w.x), a.x, acc);
+        acc = fmaf(__uint_as_float(w.y), a.y, acc);
+        acc = fmaf(__uint_as_float(w.z), a.z, acc);
+        acc = fmaf(__uint_as_float(w.w), a.w, acc);
+        return acc;
+    }
+};
+template <> struct XV<__nv_bfloat16> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float *x, int e, int plane) {
+        a = *reinterpret_cast<const float4 *>(x + (e >> 1));
+        b = *reinterpret_cast<const float4 *>(x + plane + (e >> 1));
+    }
+    // same element order as dot_x<bf16>
+    __device__ __forceinline__ float dot(const uint4 &w, float acc) const {
+        acc = fmaf(bf_lo(w.x), a.x, acc);
+        acc = fmaf(bf_hi(w.x), a.y, acc);
+        acc = fmaf(bf_lo(w.y), a.z, acc);
+        acc = fmaf(bf_hi(w.y), a.w, acc);
+        acc = fmaf(bf_lo(w.z), b.x, acc);
+        acc = fmaf(bf_hi(w.z), b.y, acc);
+        acc = fmaf(bf_lo(w.w), b.z, acc);
+        acc = fmaf(bf_hi(w.w), b.w, acc);
+        return acc;
+    }
+};
+
 // Weight rows of one problem, resolved once per segment into registers: unit u reads row
 // u of region 0 below b1, row u - b1 of region 1 below b2, else row u - b2 of region 2.
 // Gate/up and untied-head tiles read slot q < 4 from region 0 and q >= 4 from region 1
@@ -427,6 +461,72 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
             }
         }
         const int per = (r1 - r0 + GR - 1) / GR;
+        // tied LM head with one piece per row: warp q takes slot q of two consecutive tiles at
+        // once and reads each x vector once for both rows (the two right-hand sides make the
+        // head otherwise bound by shared-memory reads of x)
+        const bool pair = EPI == EPI_LM && TIED && nch == 1 && NS >= 2;
+        if constexpr (EPI == EPI_LM && TIED) {
+            if (pair) {
+                const int q = warp, plane = d >> 1, nvec = K / VEC;
+                for (int g = 0; g < per; g += 2) {
+                    const bool two = g + 1 < per;
+                    const int uA = slot_unit(r0, per, GR, q, g), uB = slot_unit(r0, per, GR, q, g + 1);
+                    const bool rvA = uA < r1, rvB = two && uB < r1;
+                    const int sA = tile % NS, sB = (tile + 1) % NS;
+                    if (!mbar_wait(&full[sA], (tile / NS) & 1)) P->st->error = ERR_TIMEOUT;
+                    if (two && !mbar_wait(&full[sB], ((tile + 1) / NS) & 1)) P->st->error = ERR_TIMEOUT;
+                    const unsigned char *tA = stages + sA * stage_bytes + q * rowb;
+                    const unsigned char *tB = stages + sB * stage_bytes + q * rowb;
+                    float cA = 0.f, eA = 0.f, cB = 0.f, eB = 0.f;
+                    for (int v = lane; v < nvec; v += 32) {
+                        XV<T> xa, xb;
+                        xa.load(xs, v * VEC, plane);
+                        xb.load(xs + d, v * VEC, plane);
+                        if (rvA) {
+                            const uint4 w = *reinterpret_cast<const uint4 *>(tA + v * 16);
+                            cA = xa.dot(w, cA);
+                            eA = xb.dot(w, eA);
+                        }
+                        if (rvB) {
+                            const uint4 w = *reinterpret_cast<const uint4 *>(tB + v * 16);
+                            cB = xa.dot(w, cB);
+                            eB = xb.dot(w, eB);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&empty[sA]);
+                        if (two) mbar_arrive(&empty[sB]);
+                    }
+                    tile += two ? 2 : 1;
+                    cA = warp_sum(cA);
+                    eA = warp_sum(eA);
+                    cB = warp_sum(cB);
+                    eB = warp_sum(eB);
+                    if (lane == 0) {
+                        for (int k = 0; k < 2; ++k) {
+                            const bool rvk = k == 0 ? rvA : rvB;
+                            if (!rvk) continue;
+                            const int unit = k == 0 ? uA : uB;
+                            const float z0 = k == 0 ? cA : cB, z1 = k == 0 ? eA : eB;
+                            P->logits[unit] = z0;
+                            P->logits[(long long)P->V + unit] = z1;
+                            if (dl) dl[unit] = z1;
+                            if (z0 > bv[0] || (z0 == bv[0] && unit < bi[0])) {
+                                bv[0] = z0;
+                                bi[0] = unit;
+                            }
+                            if (z1 > bv[1] || (z1 == bv[1] && unit < bi[1])) {
+                                bv[1] = z1;
+                                bi[1] = unit;
+                            }
+                        }
+                    }
+                }
+                r = (long long)(i + 1) * N;
+                continue;
+            }
+        }
         for (int g = 0; g < per; ++g) {
             // warp q owns tile slot q for all chunks of this group
             const int q = warp;
