@@ -101,12 +101,22 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
     __shared__ float red[40];
     __shared__ int s_done, s_t, s_head, s_ex, s_q, s_x, s_xslot, s_P0, s_newslot, s_draft, s_y, s_ok, s_active;
     __shared__ float s_tmax, s_tsum;
-    DevState *st = P->st;
+    // The slot state is small (about 1.2 KB): every thread loads a piece of it into shared
+    // memory at once, thread 0's decisions below work on that copy (no chain of dependent
+    // global loads), and all threads write it back before the next step's embedding.
+    __shared__ __align__(16) DevState sst;
+    __shared__ int s_err0;
+    static_assert(sizeof(DevState) % 16 == 0, "state copied in 16-byte words");
     const int n = P->n, ns = n + 1, V = P->V;
     const float T_ = P->temperature;
     pdl_wait();   // logits and argmax of the LM head launch
     pdl_trigger();
+    for (int i = threadIdx.x; i < (int)(sizeof(DevState) / 16); i += blockDim.x)
+        reinterpret_cast<uint4 *>(&sst)[i] = reinterpret_cast<const uint4 *>(P->st)[i];
+    __syncthreads();
+    DevState *st = &sst;
     if (threadIdx.x == 0) {
+        s_err0 = st->error;
         s_done = st->done;
         if (!s_done) {
             const int t = st->t + 1;
@@ -300,6 +310,15 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
         if (1 + st->N >= P->max_new) st->done = 1;
     }
     __syncthreads();
+    // write the state back: all 16-byte words but the first two (which hold the error
+    // word, written only if this kernel changed it), then the first eight ints
+    for (int i = 2 + threadIdx.x; i < (int)(sizeof(DevState) / 16); i += blockDim.x)
+        reinterpret_cast<uint4 *>(P->st)[i] = reinterpret_cast<const uint4 *>(&sst)[i];
+    if (threadIdx.x < 8) {
+        const int *src = reinterpret_cast<const int *>(&sst);
+        int *dst = reinterpret_cast<int *>(P->st);
+        if (threadIdx.x != 5 || sst.error != s_err0) dst[threadIdx.x] = src[threadIdx.x];
+    }
     embed_into_slot<T>(P, s_newslot, s_y);
 }
 
