@@ -317,8 +317,9 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded random-init weights drawn on the GPU, uniform-random prompt ids)",
-        "config": {"workload": f"{WL.name}: L36 d2560 32q/8kv x128 F9728 V151936, n=8, Ls=4, anchors 0,9,18,27,35, "
-                               f"prompt {WL.prompt_len}, {args.mode}",
+        "config": {"workload": f"{WL.name}: L{WL.dims.L} d{WL.dims.d} {WL.dims.Hq}q/{WL.dims.Hkv}kv x{WL.dims.hd} "
+                               f"F{WL.dims.F} V{WL.dims.V}, n={WL.n}, Ls={WL.Ls}, "
+                               f"anchors {','.join(str(a) for a in WL.anchors)}, prompt {WL.prompt_len}, {args.mode}",
                    "mode": args.mode, "n": WL.n, "prompt_len": WL.prompt_len, "max_new": r["max_new"],
                    "parallelism": f"replicas x{ws}", "l2": "no flush needed: ~9 GB of weights per step >> 129 MB L2",
                    "alpha": round(r["alpha"], 4), "S0": round(r["alpha"] * WL.n, 3),
