@@ -89,7 +89,7 @@ struct Plan {
     long long layer_bytes;         // weight bytes of one target layer
     long long pdm_bytes;           // draft module per step (projection + layers)
     long long lm_bytes;            // LM head per step
-    float *Xp, *QKVp, *ATTp, *GUp;  // draft module rows: residual, q|k|v, attention, gate|up
+    float *Xp, *QKVp, *ATTp, *GUp;  // draft module rows: residual, q|k|v, attention, SiLU(gate)*up
     float *ssp;                    // [MAXS][d / 8] sums of squares of 8-row groups of the Xp rows
     float *pdm_part;               // draft GEMM K-slab partials [slab][n+1][N]
     int *pdm_cnt;                  // draft GEMM row-block arrival counters (zero between launches)

@@ -13,8 +13,9 @@
 //   * a producer warp streams 8-row tiles of W (each row piece up to 6 KB, 1-D bulk
 //     copies) into a shared-memory ring signalled by mbarriers;
 //   * the consumer warps stage the R rows of x for the CTA's K slab in shared memory as bf16
-//     (fp32 for fp32 weights), with the input's RMS normalisation / SiLU product / anchor
-//     masking fused into the staging;
+//     (fp32 for fp32 weights), with the norm weight / anchor masking fused into the staging;
+//     an RMS-normalised input is staged as x * g and its row's 1/rms (a per-row scalar)
+//     scales the GEMM's output instead, so staging does not wait for the row statistics;
 //   * the 8 consumer warps split each tile's K range into 32-element blocks (block b to
 //     warp b mod 8); per block a warp runs two m16n8k16 tensor-core steps with the x rows
 //     as the 16-row A operand and the 8 weight rows as the B operand, both taking K in the
@@ -28,8 +29,10 @@
 // adds them in slab order and finishes the outputs.
 // Epilogues: the QKV GEMM applies RoPE and appends the rows' K,V to the module's cache
 // (a tile holds 4 rotary pairs: rows i and i + hd/2 of one head, so both halves meet in
-// one warp); projection, O and down finish residual rows and leave per-8-row sums of
-// squares for the next normalisation (independent of how CTAs split the work).
+// one warp); gate/up tiles likewise hold gate rows u..u+3 with up rows F+u..F+u+3, and the
+// epilogue leaves SiLU(gate) * up, the down GEMM's input; projection, O and down finish
+// residual rows and leave per-8-row sums of squares for the next normalisation
+// (independent of how CTAs split the work).
 #pragma once
 
 #include "common.cuh"
@@ -92,6 +95,7 @@ struct PgRows {
             const int half = hd >> 1, u = 4 * g + (q & 3), h = u / half;
             return h * hd + (u - h * half) + (q >= 4 ? half : 0);
         }
+        if (OP == OP_GATEUP) return 4 * g + (q & 3) + (q >= 4 ? b1 : 0);   // gate rows u, up rows F + u
         return 8 * g + q;
     }
     __device__ __forceinline__ const T *ptr(int row) const {
@@ -144,57 +148,67 @@ __device__ __forceinline__ void pg_store4(unsigned char *xs, int pitch, int r, i
 }
 
 // Per-row RMS statistics of Xp rows 0..R-1 from the per-8-row sums of squares that the GEMM
-// which last finished Xp left in ssp [row][d / 8] (lane-strided, then a fixed shuffle tree).
+// which last finished Xp left in ssp [row][d / 8] (lane-strided in order, then a fixed
+// shuffle tree); each lane's loads of a row are issued together.
 static __device__ __noinline__ void pg_row_inv_rms(const Plan *__restrict__ P, int R, float *inv) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ng = P->d / 8;
     for (int r = warp; r < R; r += PG_CONSUMERS / 32) {
         const float *sp = P->ssp + (long long)r * ng;
         float s = 0.f;
-        for (int c = lane; c < ng; c += 32) s += sp[c];
+        for (int c0 = 0; c0 < ng; c0 += 32 * 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int c = c0 + lane + 32 * j;
+                v[j] = c < ng ? sp[c] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s += v[j];
+        }
         s = warp_sum(s);
         if (lane == 0) inv[r] = 1.0f / sqrtf(s / (float)P->d + P->eps);
     }
 }
 
-// Stage the slab [k0, k0 + kw) of all R rows: items are 4-element groups, 8 in flight per thread.
+// Stage the slab [k0, k0 + kw) of all R rows: items are 4-element groups, U in flight per
+// thread.  Normalised inputs are staged as x * g: the row's 1/rms scales the GEMM's output.
 template <typename XT, int OP>
 static __device__ __noinline__ void pg_stage_x(const Plan *__restrict__ P, const PdmRows &pr, int layer, int k0, int kw,
-                                               unsigned char *xs, int pitch, const float *inv) {
+                                               unsigned char *xs, int pitch) {
+    constexpr bool NORM = OP == OP_QKV || OP == OP_GATEUP;
+    constexpr int U = NORM ? 8 : 16;
     const int R = pr.R, kw4 = kw >> 2, total = R * kw4, d = P->d;
     const float *g = OP == OP_QKV ? P->pl[layer].g1 : OP == OP_GATEUP ? P->pl[layer].g2 : nullptr;
-    for (int b = threadIdx.x; b < total; b += 8 * PG_CONSUMERS) {
-        float4 v[8], w[8];
+    for (int b = threadIdx.x; b < total; b += U * PG_CONSUMERS) {
+        float4 v[U], w[NORM ? U : 1];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int i = b + u * PG_CONSUMERS;
             if (i >= total) continue;
             const int r = i / kw4, k = k0 + 4 * (i - r * kw4);
             if (OP == OP_PROJ) {
+                // anchor a of the row's slot (read whatever the depth; masked below)
                 const int a = k / d, off = k - a * d;
-                v[u] = P->anchors[a] <= pr.depth[r]
-                           ? *reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + a) * d + off)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-            } else if (OP == OP_QKV || OP == OP_GATEUP) {
+                v[u] = *reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + a) * d + off);
+            } else if (NORM) {
                 v[u] = *reinterpret_cast<const float4 *>(P->Xp + (long long)r * d + k);
                 w[u] = *reinterpret_cast<const float4 *>(g + k);
             } else if (OP == OP_OPROJ) {
                 v[u] = *reinterpret_cast<const float4 *>(P->ATTp + (long long)r * P->q_rows + k);
             } else {
-                v[u] = *reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + k);
-                w[u] = *reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + P->F + k);
+                v[u] = *reinterpret_cast<const float4 *>(P->GUp + (long long)r * P->F + k);
             }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int i = b + u * PG_CONSUMERS;
             if (i >= total) continue;
             const int r = i / kw4, kk = 4 * (i - r * kw4);
             float4 x = v[u];
-            if (OP == OP_QKV || OP == OP_GATEUP) {
-                const float s = inv[r];
-                x = make_float4((x.x * s) * w[u].x, (x.y * s) * w[u].y, (x.z * s) * w[u].z, (x.w * s) * w[u].w);
-            } else if (OP == OP_DOWN) {
-                x = make_float4(silu_f(x.x) * w[u].x, silu_f(x.y) * w[u].y, silu_f(x.z) * w[u].z, silu_f(x.w) * w[u].w);
+            if (OP == OP_PROJ) {
+                if (P->anchors[(k0 + kk) / d] > pr.depth[r]) x = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (NORM) {
+                x = make_float4(x.x * w[u].x, x.y * w[u].y, x.z * w[u].z, x.w * w[u].w);
             }
             pg_store4<XT>(xs, pitch, r, kk, x);
         }
@@ -203,10 +217,14 @@ static __device__ __noinline__ void pg_stage_x(const Plan *__restrict__ P, const
 
 // Finish output (x row xr, weight row `row`, tile slot wr) of group g with value v.  Called
 // by whole warps of the reduction threads (tid < 128 MT), each thread owning the fixed
-// (xr, wr) pair of the mma fragment layout; `valid` = the pair is a real output.
+// (xr, wr) pair of the mma fragment layout; `valid` = the pair is a real output.  inv: the
+// rows' 1/rms (QKV, gate/up: their x was staged unscaled).
 template <typename T, int OP>
 __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmRows &pr, int layer, int g, int xr, int row,
-                                          int wr, float v, bool valid) {
+                                          int wr, float v, bool valid, const float *inv) {
+    if (OP == OP_QKV || OP == OP_GATEUP) {
+        if (valid) v *= inv[xr];
+    }
     if (OP == OP_QKV) {
         // rotary partner: slot wr ^ 4 of the same x row sits in lane ^ 2 (thread bit 3)
         const float partner = __shfl_xor_sync(0xffffffffu, v, 8);
@@ -225,7 +243,9 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
             reinterpret_cast<T *>(P->pvc)[cache + (row - P->q_rows - P->kv_rows)] = WTraits<T>::store(v);
         }
     } else if (OP == OP_GATEUP) {
-        if (valid) P->GUp[(long long)xr * 2 * P->F + row] = v;
+        // slots 0-3 hold gate rows u, slots 4-7 the up rows F + u, in lane ^ 2 (thread bit 3)
+        const float up = __shfl_xor_sync(0xffffffffu, v, 8);
+        if (valid && wr < 4) P->GUp[(long long)xr * P->F + row] = silu_f(v) * up;
     } else {
         float o = 0.f;
         if (valid) {
@@ -251,39 +271,33 @@ __host__ __device__ inline bool pg_xreg(int MT, int esz, int K, int ns) {
     return MT == 1 && esz == 2 && ns == 1 && K * esz <= PG_ROWB && K <= 8 * PG_XRB * PG_KB;
 }
 
-// 8 consecutive x values of row r at GEMM column k (k % 8 == 0), packed as bf16 pairs.
+// 8 consecutive x values of row r at GEMM column k (k % 8 == 0), packed as bf16 pairs
+// (normalised inputs as x * g, like the staging).
 template <int OP>
-__device__ __forceinline__ uint4 pg_x8(const Plan *__restrict__ P, const PdmRows &pr, int layer, int r, int k,
-                                       const float *inv) {
+__device__ __forceinline__ uint4 pg_x8(const Plan *__restrict__ P, const PdmRows &pr, int layer, int r, int k) {
     const int d = P->d;
     float4 a, b;
     if (OP == OP_PROJ) {
         const int an = k / d, off = k - an * d;
-        if (P->anchors[an] <= pr.depth[r]) {
-            const float4 *src = reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + an) * d + off);
-            a = src[0];
-            b = src[1];
-        } else {
-            a = b = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        const float4 *src = reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + an) * d + off);
+        a = src[0];
+        b = src[1];
+        if (P->anchors[an] > pr.depth[r]) a = b = make_float4(0.f, 0.f, 0.f, 0.f);
     } else if (OP == OP_QKV || OP == OP_GATEUP) {
         const float *g = OP == OP_QKV ? P->pl[layer].g1 : P->pl[layer].g2;
         const float4 *src = reinterpret_cast<const float4 *>(P->Xp + (long long)r * d + k);
         const float4 x0 = src[0], x1 = src[1];
         const float4 g0 = *reinterpret_cast<const float4 *>(g + k), g1 = *reinterpret_cast<const float4 *>(g + k + 4);
-        const float s = inv[r];
-        a = make_float4((x0.x * s) * g0.x, (x0.y * s) * g0.y, (x0.z * s) * g0.z, (x0.w * s) * g0.w);
-        b = make_float4((x1.x * s) * g1.x, (x1.y * s) * g1.y, (x1.z * s) * g1.z, (x1.w * s) * g1.w);
+        a = make_float4(x0.x * g0.x, x0.y * g0.y, x0.z * g0.z, x0.w * g0.w);
+        b = make_float4(x1.x * g1.x, x1.y * g1.y, x1.z * g1.z, x1.w * g1.w);
     } else if (OP == OP_OPROJ) {
         const float4 *src = reinterpret_cast<const float4 *>(P->ATTp + (long long)r * P->q_rows + k);
         a = src[0];
         b = src[1];
     } else {
-        const float4 *gs = reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + k);
-        const float4 *us = reinterpret_cast<const float4 *>(P->GUp + (long long)r * 2 * P->F + P->F + k);
-        const float4 g0 = gs[0], g1 = gs[1], u0 = us[0], u1 = us[1];
-        a = make_float4(silu_f(g0.x) * u0.x, silu_f(g0.y) * u0.y, silu_f(g0.z) * u0.z, silu_f(g0.w) * u0.w);
-        b = make_float4(silu_f(g1.x) * u1.x, silu_f(g1.y) * u1.y, silu_f(g1.z) * u1.z, silu_f(g1.w) * u1.w);
+        const float4 *src = reinterpret_cast<const float4 *>(P->GUp + (long long)r * P->F + k);
+        a = src[0];
+        b = src[1];
     }
     __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
     __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
@@ -345,10 +359,6 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // ------------------------------ consumers -------------------------------------------
     pdl_wait();   // x, its statistics and the counters belong to the preceding launch
     pdl_trigger();
-    if (OP == OP_QKV || OP == OP_GATEUP) {
-        pg_row_inv_rms(P, R, s_inv);
-        named_sync(PG_BAR, PG_CONSUMERS);
-    }
     // register-resident x (bf16, one mma tile): lane (gq, tq) of warp w holds rows gq and gq + 8,
     // elements 8tq..8tq+7 of blocks w, w + 8, ... of the GEMM's K
     uint4 xf[PG_XRB][2];
@@ -358,15 +368,15 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
 #pragma unroll
             for (int j = 0; j < PG_XRB; ++j) {
                 const int bb = warp + 8 * j, k = k0 + bb * PG_KB + 8 * tq;
-                xf[j][0] = bb < nblk && gq < R ? pg_x8<OP>(P, pr, layer, gq, k, s_inv) : make_uint4(0u, 0u, 0u, 0u);
-                xf[j][1] = bb < nblk && gq + 8 < R ? pg_x8<OP>(P, pr, layer, gq + 8, k, s_inv) : make_uint4(0u, 0u, 0u, 0u);
+                xf[j][0] = bb < nblk && gq < R ? pg_x8<OP>(P, pr, layer, gq, k) : make_uint4(0u, 0u, 0u, 0u);
+                xf[j][1] = bb < nblk && gq + 8 < R ? pg_x8<OP>(P, pr, layer, gq + 8, k) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
     }
-    if (!xreg) {
-        pg_stage_x<T, OP>(P, pr, layer, k0, kw, xs, xpitch, s_inv);
-        named_sync(PG_BAR, PG_CONSUMERS);
-    }
+    if (!xreg) pg_stage_x<T, OP>(P, pr, layer, k0, kw, xs, xpitch);
+    // the rows' 1/rms (read by the epilogue, after the first group's barrier at the latest)
+    if (OP == OP_QKV || OP == OP_GATEUP) pg_row_inv_rms(P, R, s_inv);
+    if (!xreg) named_sync(PG_BAR, PG_CONSUMERS);
 
     // reduction thread t (< 128 MT) owns x row xr_t and tile slot wr_t of every group
     const int rm = tid >> 7, rl = (tid >> 2) & 31, rreg = tid & 3;
@@ -483,7 +493,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
 #pragma unroll
             for (int w = 0; w < PG_CONSUMERS / 32; ++w) s += rf[(((buf * (PG_CONSUMERS / 32) + w) * MT + rm) * 32 + rl) * 4 + rreg];
             const int row = wrows.row_of(g, wr_t);
-            if (ns == 1) pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R);
+            if (ns == 1) pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R, s_inv);
             else if (xr_t < R) part[((long long)sl * (P->n + 1) + xr_t) * N + row] = s;
         }
         buf ^= 1;
@@ -529,7 +539,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
             for (int f = 0; f < PG_FIN; ++f) {
                 const int g = g0 + f * GPP + gsub;
                 // warp-uniform: the 32 threads of a warp share gsub, hence g
-                if (g < gb1) pg_finish<T, OP>(P, pr, layer, g, xr, wrows.row_of(g, wr), wr, sum[f], xr < R);
+                if (g < gb1) pg_finish<T, OP>(P, pr, layer, g, xr, wrows.row_of(g, wr), wr, sum[f], xr < R, s_inv);
             }
         }
     }
