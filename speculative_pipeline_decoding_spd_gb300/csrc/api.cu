@@ -126,6 +126,9 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.QKVp = b.take<float>((size_t)ns * qkv);
     h.ATTp = b.take<float>((size_t)ns * qr);
     h.GUp = b.take<float>((size_t)ns * d->F);
+    h.Xb = b.take<__nv_bfloat16>((size_t)ns * d->d);
+    h.ATTb = b.take<__nv_bfloat16>((size_t)ns * qr);
+    h.GUb = b.take<__nv_bfloat16>((size_t)ns * d->F);
     h.ssp = b.take<float>((size_t)MAXS * (d->d / 8));
     {
         // draft GEMM K-slab partials: largest slabs x rows x outputs over the five GEMMs

@@ -75,7 +75,14 @@ struct AttnArgs {
                              // no merge here, every chunk (even a single one) leaves its partial
     int prob, maxch, Hq, Hkv, hd;
     float scale;
+    __nv_bfloat16 *outb;     // if set, the output goes here as bf16 instead of to out
 };
+
+template <typename T>
+__device__ __forceinline__ void attn_store_out(const AttnArgs<T> &a, long long i, float v) {
+    if (a.outb) a.outb[i] = __float2bfloat16_rn(v);
+    else a.out[i] = v;
+}
 
 // The work of CTA (kv head g, chunk c) for one problem, plus the merge when this CTA is
 // the last of its (problem, kv head).  Block-uniform: every thread of the CTA calls it.
@@ -281,7 +288,7 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
             float oo = ored[u * hd + dd];
             for (int w = 1; w < ATT_THREADS / 32; ++w) oo += ored[(w * ATT_HB + u) * hd + dd];
             if (nch == 1 && a.cnt) {
-                a.out[(long long)(g * G + h) * hd + dd] = oo / s_l[h];
+                attn_store_out(a, (long long)(g * G + h) * hd + dd, oo / s_l[h]);
             } else {
                 a.part[pidx(h, c) + dd] = oo;
                 if (dd == 0) {
@@ -337,7 +344,7 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
             for (int u = 0; u < 8; ++u)
                 if (c0 + u < nch) num = fmaf(mw[h * ATT_CHUNK + c0 + u], vals[u], num);
         }
-        a.out[(long long)(g * G + h) * hd + dd] = num / s_l[h];
+        attn_store_out(a, (long long)(g * G + h) * hd + dd, num / s_l[h]);
     }
     if (tid == 0) *cntp = 0;
 }

@@ -91,6 +91,10 @@ struct Plan {
     long long lm_bytes;            // LM head per step
     float *Xp, *QKVp, *ATTp, *GUp;  // draft module rows: residual, q|k|v, attention, SiLU(gate)*up
     float *ssp;                    // [MAXS][d / 8] sums of squares of 8-row groups of the Xp rows
+    // bf16 weights: the draft GEMMs' inputs as bf16 rows, copied into shared memory whole
+    __nv_bfloat16 *Xb;             // [n+1][d] Xp * g of the next normalisation (1/rms applied after the GEMM)
+    __nv_bfloat16 *ATTb;           // [n+1][Hq hd] attention output
+    __nv_bfloat16 *GUb;            // [n+1][F] SiLU(gate) * up
     float *pdm_part;               // draft GEMM K-slab partials [slab][n+1][N]
     int *pdm_cnt;                  // draft GEMM row-block arrival counters (zero between launches)
     int pdm_kx[5], pdm_ns[5];      // draft GEMMs (proj, qkv, o, gate/up, down): K slab width, slabs
@@ -152,6 +156,8 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
+// Orders this thread's generic-proxy memory accesses before its later bulk copies.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
 // Asynchronous 16-byte global -> shared copy (no register staging); wait_all waits for all
 // of the thread's outstanding copies.
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {

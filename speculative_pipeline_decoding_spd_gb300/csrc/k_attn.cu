@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const
     __syncthreads();
     if (!s_ok) return;
     if (!TARGET) pdl_wait();   // the rows' K,V were appended by the preceding draft QKV launch
-    AttnArgs<T> a;
+    AttnArgs<T> a{};
     const long long kvoff = (long long)s_layer * P->kv_stride;
     a.kc = reinterpret_cast<T *>(TARGET ? P->kc : P->pkc) + kvoff;
     a.vc = reinterpret_cast<T *>(TARGET ? P->vc : P->pvc) + kvoff;
@@ -78,7 +78,9 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const
         a.rope = nullptr;
         a.kraw = nullptr;
         a.vraw = nullptr;
-        a.out = P->ATTp + (long long)s_src * P->q_rows;
+        // bf16 weights: the O GEMM copies its input rows as bf16
+        if (sizeof(T) == 2) a.outb = P->ATTb + (long long)s_src * P->q_rows;
+        else a.out = P->ATTp + (long long)s_src * P->q_rows;
         a.part = P->patt_part;
         a.cnt = P->patt_cnt;
         a.prob = s_src;

@@ -11,7 +11,7 @@ namespace spd {
 template <typename T, int OP, int MT>
 __global__ void __launch_bounds__(PG_THREADS, 1) k_pdm_gemm(const Plan *__restrict__ P, int layer) {
     extern __shared__ __align__(128) unsigned char pg_smem[];
-    __shared__ __align__(8) uint64_t full[PG_MAXNS], empty[PG_MAXNS];
+    __shared__ __align__(8) uint64_t full[PG_MAXNS], empty[PG_MAXNS], xbar;
     __shared__ PdmRows pr;
     __shared__ float s_inv[MAXS];
     __shared__ int s_done, s_flag;
@@ -22,12 +22,13 @@ __global__ void __launch_bounds__(PG_THREADS, 1) k_pdm_gemm(const Plan *__restri
                 mbar_init(&full[i], 1);
                 mbar_init(&empty[i], PG_CONSUMERS / 32);
             }
+            mbar_init(&xbar, 1);
             fence_mbar_init();
         }
     }
     __syncthreads();
     if (s_done) return;
-    pdm_gemm_cta<T, OP, MT>(P, pr, layer, blockIdx.x, gridDim.x, pg_smem, full, empty, s_inv, &s_flag);
+    pdm_gemm_cta<T, OP, MT>(P, pr, layer, blockIdx.x, gridDim.x, pg_smem, full, empty, &xbar, s_inv, &s_flag);
 }
 
 // ---------------------------------------------------------------------------------

@@ -46,7 +46,7 @@ constexpr int PG_THREADS = PG_CONSUMERS + 32;  // + 1 producer warp
 constexpr int PG_RG = 8;                       // weight rows per tile (the mma's n)
 constexpr int PG_ROWB = 6144;                  // bytes of one row per tile piece, at most
 constexpr int PG_MAXNS = 8;                    // ring stages at most
-constexpr int PG_SMEM = 210 * 1024;            // x + reduction buffers + ring
+constexpr int PG_SMEM = 224 * 1024;            // x + reduction buffers + ring
 constexpr int PG_XMAX = 48 * 1024;             // budget of the x rows of one slab
 constexpr int PG_XRB = 10;                     // register-resident x: 32-element blocks per warp, at most
 constexpr int PG_KB = 32;                      // K elements per warp block
@@ -245,13 +245,24 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
     } else if (OP == OP_GATEUP) {
         // slots 0-3 hold gate rows u, slots 4-7 the up rows F + u, in lane ^ 2 (thread bit 3)
         const float up = __shfl_xor_sync(0xffffffffu, v, 8);
-        if (valid && wr < 4) P->GUp[(long long)xr * P->F + row] = silu_f(v) * up;
+        if (valid && wr < 4) {
+            const float h = silu_f(v) * up;
+            if (sizeof(T) == 2) P->GUb[(long long)xr * P->F + row] = __float2bfloat16_rn(h);
+            else P->GUp[(long long)xr * P->F + row] = h;
+        }
     } else {
         float o = 0.f;
         if (valid) {
             float *dst = P->Xp + (long long)xr * P->d + row;
             o = OP == OP_PROJ ? v : *dst + v;
             *dst = o;
+            if (sizeof(T) == 2) {
+                // bf16 input row of the next GEMM: x * g of its normalisation (none after the
+                // last layer: the LM head normalises Xp itself)
+                const float *gn = OP == OP_PROJ ? P->pl[0].g1 : OP == OP_OPROJ ? P->pl[layer].g2
+                                : layer + 1 < P->Ls ? P->pl[layer + 1].g1 : nullptr;
+                if (gn) P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * gn[row]);
+            }
         }
         // sum of squares of the 8 rows of this group for x row xr (lanes differing in thread
         // bits 0, 2, 3 hold its 8 weight rows)
@@ -307,11 +318,13 @@ __device__ __forceinline__ uint4 pg_x8(const Plan *__restrict__ P, const PdmRows
 
 // One CTA's share of a draft GEMM: CTA p of m_pdm (row block p / ns, K slab p % ns).
 // smem: the dynamic shared memory; full/empty: PG_MAXNS mbarriers each, initialised (full
-// count 1, empty count 8) and fenced by the caller; s_inv: MAXS floats.  Called by all
+// count 1, empty count 8) and fenced by the caller, like xbar (count 1: the bf16 x rows'
+// copies); s_inv: MAXS floats.  Called by all
 // PG_THREADS threads (warp 8 is the producer); returns when the CTA's work is done.
 template <typename T, int OP, int MT>
 __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int layer, int p, int m_pdm,
-                             unsigned char *smem, uint64_t *full, uint64_t *empty, float *s_inv, int *s_flag) {
+                             unsigned char *smem, uint64_t *full, uint64_t *empty, uint64_t *xbar, float *s_inv,
+                             int *s_flag) {
     constexpr int ESZ = sizeof(T);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int ns = P->pdm_ns[OP], kx = P->pdm_kx[OP];
@@ -325,7 +338,11 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     const int xpitch = pg_pitch(kx, ESZ);
     const int rowb = pg_pitch(KC, ESZ), stage_bytes = PG_RG * rowb;
     const bool xreg = pg_xreg(MT, ESZ, K, ns);
-    const int xbytes = xreg ? 0 : pg_xbytes(P->n + 1, kx, ESZ);
+    // bf16 weights: the inputs (except the projection's masked anchors) are bf16 rows in
+    // global memory already, copied whole into x by bulk copies; the register-resident
+    // fragments are then read from there
+    constexpr bool BULK = ESZ == 2 && OP != OP_PROJ;
+    const int xbytes = xreg && !BULK ? 0 : pg_xbytes(P->n + 1, kx, ESZ);
     unsigned char *xs = smem;
     float4 *red = reinterpret_cast<float4 *>(smem + xbytes);
     unsigned char *stages = smem + xbytes + pg_redbytes(MT);
@@ -359,24 +376,44 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // ------------------------------ consumers -------------------------------------------
     pdl_wait();   // x, its statistics and the counters belong to the preceding launch
     pdl_trigger();
+    if constexpr (BULK) {
+        if (tid == 0) {
+            const __nv_bfloat16 *src = OP == OP_OPROJ ? P->ATTb : OP == OP_DOWN ? P->GUb : P->Xb;
+            const uint32_t rb = (uint32_t)kw * 2;
+            fence_proxy_async();
+            mbar_expect_tx(xbar, rb * R);
+            for (int r = 0; r < R; ++r) bulk_g2s(xs + r * xpitch, src + (long long)r * K + k0, rb, xbar);
+        }
+    } else if (!xreg) {
+        pg_stage_x<T, OP>(P, pr, layer, k0, kw, xs, xpitch);
+    }
+    // the rows' 1/rms (read by the epilogue, after the first group's barrier at the latest)
+    if (OP == OP_QKV || OP == OP_GATEUP) pg_row_inv_rms(P, R, s_inv);
+    if constexpr (BULK) {
+        if (!mbar_wait(xbar, 0)) P->st->error = ERR_TIMEOUT;
+    } else if (!xreg) {
+        named_sync(PG_BAR, PG_CONSUMERS);
+    }
     // register-resident x (bf16, one mma tile): lane (gq, tq) of warp w holds rows gq and gq + 8,
     // elements 8tq..8tq+7 of blocks w, w + 8, ... of the GEMM's K
     uint4 xf[PG_XRB][2];
     if constexpr (ESZ == 2 && MT == 1) {
         if (xreg) {
             const int gq = lane >> 2, tq = lane & 3, nblk = kw / PG_KB;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int j = 0; j < PG_XRB; ++j) {
-                const int bb = warp + 8 * j, k = k0 + bb * PG_KB + 8 * tq;
-                xf[j][0] = bb < nblk && gq < R ? pg_x8<OP>(P, pr, layer, gq, k) : make_uint4(0u, 0u, 0u, 0u);
-                xf[j][1] = bb < nblk && gq + 8 < R ? pg_x8<OP>(P, pr, layer, gq + 8, k) : make_uint4(0u, 0u, 0u, 0u);
+                const int bb = warp + 8 * j, kl = bb * PG_KB + 8 * tq;
+                if constexpr (BULK) {
+                    xf[j][0] = bb < nblk && gq < R ? lds128(xs + gq * xpitch + kl * 2) : z;
+                    xf[j][1] = bb < nblk && gq + 8 < R ? lds128(xs + (gq + 8) * xpitch + kl * 2) : z;
+                } else {
+                    xf[j][0] = bb < nblk && gq < R ? pg_x8<OP>(P, pr, layer, gq, k0 + kl) : z;
+                    xf[j][1] = bb < nblk && gq + 8 < R ? pg_x8<OP>(P, pr, layer, gq + 8, k0 + kl) : z;
+                }
             }
         }
     }
-    if (!xreg) pg_stage_x<T, OP>(P, pr, layer, k0, kw, xs, xpitch);
-    // the rows' 1/rms (read by the epilogue, after the first group's barrier at the latest)
-    if (OP == OP_QKV || OP == OP_GATEUP) pg_row_inv_rms(P, R, s_inv);
-    if (!xreg) named_sync(PG_BAR, PG_CONSUMERS);
 
     // reduction thread t (< 128 MT) owns x row xr_t and tile slot wr_t of every group
     const int rm = tid >> 7, rl = (tid >> 2) & 31, rreg = tid & 3;
