@@ -532,6 +532,10 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
             const int q = warp;
             const int unit = slot_unit(r0, per, GR, q, g);
             const bool rv = unit < r1;
+            // the residual this row adds to, loaded before the dot product so that its latency
+            // overlaps the tile instead of stalling the warp after it
+            float xold = 0.f;
+            if ((EPI == EPI_OPROJ || EPI == EPI_DOWN) && lane == 0 && rv) xold = P->X[(long long)slot * d + unit];
             float acc0 = 0.f, acc1 = 0.f;
             for (int c = 0; c < nch; ++c) {
                 const int kc0 = c * KC, len = min(KC, K - kc0);
@@ -578,15 +582,14 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                 if (EPI == EPI_QKV) {
                     P->QKV[(long long)s * P->qkv_rows + unit] = acc0;
                 } else if (EPI == EPI_OPROJ) {
-                    P->X[(long long)slot * d + unit] += acc0;
+                    P->X[(long long)slot * d + unit] = xold + acc0;
                 } else if (EPI == EPI_GATEUP) {
                     // raw gate (rows 0..3) and up (rows 4..7) sums; SiLU(gate) * up is formed when
                     // the down projection stages its input
                     P->U[(long long)s * 2 * P->F + (q < 4 ? 0 : P->F) + unit] = acc0;
                 } else if (EPI == EPI_DOWN) {
-                    float *xp = P->X + (long long)slot * d + unit;
-                    const float xn = *xp + acc0;
-                    *xp = xn;
+                    const float xn = xold + acc0;
+                    P->X[(long long)slot * d + unit] = xn;
                     const int a = P->aidx[layer + 1];
                     if (a >= 0) P->ANCH[((long long)slot * P->nB + a) * d + unit] = xn;
                 } else {

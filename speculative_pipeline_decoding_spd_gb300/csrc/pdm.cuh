@@ -215,13 +215,37 @@ static __device__ __noinline__ void pg_stage_x(const Plan *__restrict__ P, const
     }
 }
 
+// The global values that the epilogue of output (x row xr, weight row `row`, tile slot wr)
+// reads, loaded ahead of it so that their latency overlaps the GEMM: QKV: the rotation's
+// (cos, sin); projection, O, down: (residual, weight of the next normalisation).
+template <typename T, int OP>
+__device__ __forceinline__ float2 pg_prefetch(const Plan *__restrict__ P, const PdmRows &pr, int layer, int xr, int row,
+                                              int wr, bool valid) {
+    float2 r = make_float2(0.f, 0.f);
+    if (!valid) return r;
+    if (OP == OP_QKV) {
+        if (row < P->q_rows + P->kv_rows) {
+            const int pos = pr.pos0 + xr, hd = P->hd, half = hd >> 1, i = row % hd;
+            r = P->rope[(long long)pos * half + (wr < 4 ? i : i - half)];
+        }
+    } else if (OP != OP_GATEUP) {
+        if (OP != OP_PROJ) r.x = P->Xp[(long long)xr * P->d + row];
+        if (sizeof(T) == 2) {
+            const float *gn = OP == OP_PROJ ? P->pl[0].g1 : OP == OP_OPROJ ? P->pl[layer].g2
+                            : layer + 1 < P->Ls ? P->pl[layer + 1].g1 : nullptr;
+            if (gn) r.y = gn[row];
+        }
+    }
+    return r;
+}
+
 // Finish output (x row xr, weight row `row`, tile slot wr) of group g with value v.  Called
 // by whole warps of the reduction threads (tid < 128 MT), each thread owning the fixed
 // (xr, wr) pair of the mma fragment layout; `valid` = the pair is a real output.  inv: the
-// rows' 1/rms (QKV, gate/up: their x was staged unscaled).
+// rows' 1/rms (QKV, gate/up: their x was staged unscaled); pre: pg_prefetch's values.
 template <typename T, int OP>
 __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmRows &pr, int layer, int g, int xr, int row,
-                                          int wr, float v, bool valid, const float *inv) {
+                                          int wr, float v, bool valid, const float *inv, float2 pre) {
     if (OP == OP_QKV || OP == OP_GATEUP) {
         if (valid) v *= inv[xr];
     }
@@ -229,12 +253,11 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
         // rotary partner: slot wr ^ 4 of the same x row sits in lane ^ 2 (thread bit 3)
         const float partner = __shfl_xor_sync(0xffffffffu, v, 8);
         if (!valid) return;
-        const int pos = pr.pos0 + xr, hd = P->hd, half = hd >> 1;
+        const int pos = pr.pos0 + xr;
         const long long cache = (long long)layer * P->kv_stride + (long long)pos * P->kv_rows;
         if (row < P->q_rows + P->kv_rows) {
             const bool first = wr < 4;
-            const int i = row % hd, j = first ? i : i - half;
-            const float2 cs = P->rope[(long long)pos * half + j];
+            const float2 cs = pre;
             const float a = first ? v : partner, b = first ? partner : v;
             const float y = first ? a * cs.x - b * cs.y : b * cs.x + a * cs.y;
             if (row < P->q_rows) P->QKVp[(long long)xr * P->qkv_rows + row] = y;
@@ -253,16 +276,12 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
     } else {
         float o = 0.f;
         if (valid) {
-            float *dst = P->Xp + (long long)xr * P->d + row;
-            o = OP == OP_PROJ ? v : *dst + v;
-            *dst = o;
-            if (sizeof(T) == 2) {
-                // bf16 input row of the next GEMM: x * g of its normalisation (none after the
-                // last layer: the LM head normalises Xp itself)
-                const float *gn = OP == OP_PROJ ? P->pl[0].g1 : OP == OP_OPROJ ? P->pl[layer].g2
-                                : layer + 1 < P->Ls ? P->pl[layer + 1].g1 : nullptr;
-                if (gn) P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * gn[row]);
-            }
+            o = OP == OP_PROJ ? v : pre.x + v;
+            P->Xp[(long long)xr * P->d + row] = o;
+            // bf16 input row of the next GEMM: x * g of its normalisation (none after the last
+            // layer: the LM head normalises Xp itself)
+            if (sizeof(T) == 2 && (OP != OP_DOWN || layer + 1 < P->Ls))
+                P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * pre.y);
         }
         // sum of squares of the 8 rows of this group for x row xr (lanes differing in thread
         // bits 0, 2, 3 hold its 8 weight rows)
@@ -423,6 +442,8 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     uint32_t tile = 0;
     int buf = 0;
     for (int g = gb0; g < gb1; ++g) {
+        float2 pre = make_float2(0.f, 0.f);
+        if (ns == 1 && tid < 128 * MT) pre = pg_prefetch<T, OP>(P, pr, layer, xr_t, wrows.row_of(g, wr_t), wr_t, xr_t < R);
         // bf16: acc[4m..4m+3] is the m-th 16x8 mma accumulator fragment; fp32: acc[j] is the
         // (x row (lane >> 3) + 4j, tile slot lane & 7) product
         float acc[4 * MT];
@@ -530,7 +551,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
 #pragma unroll
             for (int w = 0; w < PG_CONSUMERS / 32; ++w) s += rf[(((buf * (PG_CONSUMERS / 32) + w) * MT + rm) * 32 + rl) * 4 + rreg];
             const int row = wrows.row_of(g, wr_t);
-            if (ns == 1) pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R, s_inv);
+            if (ns == 1) pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R, s_inv, pre);
             else if (xr_t < R) part[((long long)sl * (P->n + 1) + xr_t) * N + row] = s;
         }
         buf ^= 1;
@@ -553,8 +574,13 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
         const int xr = (t >> 7) * 16 + ((t & 3) >> 1) * 8 + ((t >> 2) & 31) / 4, wr = (((t >> 2) & 31) & 3) * 2 + (t & 1);
         for (int g0 = gb0; g0 < gb1; g0 += GPP * PG_FIN) {
             float sum[PG_FIN];
+            float2 pre[PG_FIN];
 #pragma unroll
-            for (int f = 0; f < PG_FIN; ++f) sum[f] = 0.f;
+            for (int f = 0; f < PG_FIN; ++f) {
+                sum[f] = 0.f;
+                const int g = g0 + f * GPP + gsub;
+                pre[f] = pg_prefetch<T, OP>(P, pr, layer, xr, wrows.row_of(min(g, gb1 - 1), wr), wr, g < gb1 && xr < R);
+            }
             for (int s0 = 0; s0 < ns; s0 += 4) {
                 float v[PG_FIN][4];
 #pragma unroll
@@ -576,7 +602,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
             for (int f = 0; f < PG_FIN; ++f) {
                 const int g = g0 + f * GPP + gsub;
                 // warp-uniform: the 32 threads of a warp share gsub, hence g
-                if (g < gb1) pg_finish<T, OP>(P, pr, layer, g, xr, wrows.row_of(g, wr), wr, sum[f], xr < R, s_inv);
+                if (g < gb1) pg_finish<T, OP>(P, pr, layer, g, xr, wrows.row_of(g, wr), wr, sum[f], xr < R, s_inv, pre[f]);
             }
         }
     }
