@@ -129,10 +129,11 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.Xb = b.take<__nv_bfloat16>((size_t)ns * d->d);
     h.ATTb = b.take<__nv_bfloat16>((size_t)ns * qr);
     h.GUb = b.take<__nv_bfloat16>((size_t)ns * d->F);
+    h.Xlm = b.take<__nv_bfloat16>((size_t)2 * d->d);
     h.ssp = b.take<float>((size_t)MAXS * (d->d / 8));
     {
         // draft GEMM K-slab partials: largest slabs x rows x outputs over the five GEMMs
-        int kx[5], nsl[5], MT;
+        int kx[6], nsl[6], MT;
         pdm_plan(d->d, d->F, qr, c->n_anchors, n, d->dtype, kx, nsl, &MT);
         const int Ns[5] = {d->d, qkv, d->d, 2 * d->F, d->d};
         size_t most = 1;
@@ -377,7 +378,8 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
         cudaMemsetAsync(h.att_cnt, 0, sizeof(int) * MAXS * h.Hkv, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.patt_cnt, 0, sizeof(int) * MAXS * h.Hkv, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.pdm_cnt, 0, sizeof(int) * SM_BOUND, H->s_main) != cudaSuccess ||
-        cudaMemsetAsync(h.lm_cnt, 0, sizeof(int), H->s_main) != cudaSuccess) {
+        cudaMemsetAsync(h.lm_cnt, 0, sizeof(int), H->s_main) != cudaSuccess ||
+        cudaMemsetAsync(h.Xlm, 0, sizeof(__nv_bfloat16) * 2 * h.d, H->s_main) != cudaSuccess) {
         H->err = "workspace initialisation failed";
         return bail(SPD_ECUDA);
     }

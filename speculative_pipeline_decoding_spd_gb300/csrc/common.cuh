@@ -95,9 +95,10 @@ struct Plan {
     __nv_bfloat16 *Xb;             // [n+1][d] Xp * g of the next normalisation (1/rms applied after the GEMM)
     __nv_bfloat16 *ATTb;           // [n+1][Hq hd] attention output
     __nv_bfloat16 *GUb;            // [n+1][F] SiLU(gate) * up
+    __nv_bfloat16 *Xlm;            // [2][d] LM head rows: x * g_final of the exiting token and of the draft's newest row
     float *pdm_part;               // draft GEMM K-slab partials [slab][n+1][N]
     int *pdm_cnt;                  // draft GEMM row-block arrival counters (zero between launches)
-    int pdm_kx[5], pdm_ns[5];      // draft GEMMs (proj, qkv, o, gate/up, down): K slab width, slabs
+    int pdm_kx[6], pdm_ns[6];      // draft-style GEMMs (proj, qkv, o, gate/up, down, LM head): K slab width, slabs
     int pdm_MT;                    // 16-row mma tiles of the draft rows (1: n+1 <= 16, else 2)
     int pdl;                       // step kernels launched with programmatic dependent launch
     float *logits;                 // [2][V]
@@ -471,7 +472,9 @@ template <typename T> void launch_target_down(const Plan *P, const Plan &h, int 
 template <typename T> void launch_lm_head(const Plan *P, const Plan &h, int grid, cudaStream_t s);
 template <typename T> void launch_pdm_step(const Plan *P, const Plan &h, int grid, cudaStream_t s);
 template <typename T> void launch_pdm_attn(const Plan *P, const Plan &h, int layer, cudaStream_t s);
-void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[5], int ns[5], int *MT);
+void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[6], int ns[6], int *MT);
+template <typename T> void launch_pdm_lm(const Plan *P, const Plan &h, int grid, cudaStream_t s);
+bool lm_on_tensor_cores(const Plan &h);   // the LM head runs as a tensor-core GEMM (launch_pdm_lm)
 void set_pdm_attributes();
 void set_target_attributes(int smem);
 void set_prefill_attributes();

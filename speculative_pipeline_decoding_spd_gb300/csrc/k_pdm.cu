@@ -43,12 +43,12 @@ static int pg_slab(int K, int rows, int esz) {
     return kx;
 }
 
-void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[5], int ns[5], int *MT) {
+void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[6], int ns[6], int *MT) {
     const int esz = dtype == SPD_BF16 ? 2 : 4, rows = n + 1;
     *MT = rows <= 16 ? 1 : 2;
-    const int Ks[5] = {nB * d, d, q_rows, d, F};
-    for (int i = 0; i < 5; ++i) {
-        kx[i] = pg_slab(Ks[i], rows, esz);
+    const int Ks[6] = {nB * d, d, q_rows, d, F, d};
+    for (int i = 0; i < 6; ++i) {
+        kx[i] = pg_slab(Ks[i], i == OP_LM ? 2 : rows, esz);
         ns[i] = (Ks[i] + kx[i] - 1) / kx[i];
     }
 }
@@ -72,6 +72,16 @@ static void pdm_step_mt(const Plan *P, const Plan &h, int grid, cudaStream_t s) 
     }
 }
 
+// The tied bf16 LM head (two rows, one K slab: V % 8 == 0 and x of both rows in shared memory).
+bool lm_on_tensor_cores(const Plan &h) {
+    return h.dtype == SPD_BF16 && h.pdm_lm_head == h.lm_head && h.V % 8 == 0 && h.pdm_ns[OP_LM] == 1;
+}
+
+template <typename T>
+void launch_pdm_lm(const Plan *P, const Plan &h, int grid, cudaStream_t s) {
+    launch_k(k_pdm_gemm<T, OP_LM, 1>, dim3(grid), dim3(PG_THREADS), PG_SMEM, s, h.pdl != 0, P, 0);
+}
+
 template <typename T>
 void launch_pdm_step(const Plan *P, const Plan &h, int grid, cudaStream_t s) {
     if (h.pdm_MT == 1) pdm_step_mt<T, 1>(P, h, grid, s);
@@ -88,6 +98,8 @@ static void set_attr_mt() {
 }
 
 void set_pdm_attributes() {
+    cudaFuncSetAttribute(k_pdm_gemm<float, OP_LM, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
+    cudaFuncSetAttribute(k_pdm_gemm<__nv_bfloat16, OP_LM, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PG_SMEM);
     set_attr_mt<float, 1>();
     set_attr_mt<float, 2>();
     set_attr_mt<__nv_bfloat16, 1>();
@@ -95,6 +107,8 @@ void set_pdm_attributes() {
 }
 
 template void launch_pdm_step<float>(const Plan *, const Plan &, int, cudaStream_t);
+template void launch_pdm_lm<float>(const Plan *, const Plan &, int, cudaStream_t);
+template void launch_pdm_lm<__nv_bfloat16>(const Plan *, const Plan &, int, cudaStream_t);
 template void launch_pdm_step<__nv_bfloat16>(const Plan *, const Plan &, int, cudaStream_t);
 
 }  // namespace spd

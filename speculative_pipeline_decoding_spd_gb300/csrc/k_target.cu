@@ -534,8 +534,11 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
             const bool rv = unit < r1;
             // the residual this row adds to, loaded before the dot product so that its latency
             // overlaps the tile instead of stalling the warp after it
-            float xold = 0.f;
+            float xold = 0.f, gfin = 0.f;
             if ((EPI == EPI_OPROJ || EPI == EPI_DOWN) && lane == 0 && rv) xold = P->X[(long long)slot * d + unit];
+            // the last layer's output is also the LM head's bf16 input row x * g_final
+            const bool lm_row = EPI == EPI_DOWN && sizeof(T) == 2 && layer + 1 == P->L;
+            if (lm_row && lane == 0 && rv) gfin = P->gf[unit];
             float acc0 = 0.f, acc1 = 0.f;
             for (int c = 0; c < nch; ++c) {
                 const int kc0 = c * KC, len = min(KC, K - kc0);
@@ -592,6 +595,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                     P->X[(long long)slot * d + unit] = xn;
                     const int a = P->aidx[layer + 1];
                     if (a >= 0) P->ANCH[((long long)slot * P->nB + a) * d + unit] = xn;
+                    if (lm_row) P->Xlm[unit] = __float2bfloat16_rn(xn * gfin);
                 } else {
                     // logits: tied -> both rows of this vocab id; untied -> row (q >= 4) only
                     const int h0 = TIED ? 0 : (q < 4 ? 0 : 1);
@@ -707,6 +711,10 @@ void launch_target_down(const Plan *P, const Plan &h, int round, int grid, cudaS
 }
 template <typename T>
 void launch_lm_head(const Plan *P, const Plan &h, int grid, cudaStream_t s) {
+    if (lm_on_tensor_cores(h)) {
+        launch_pdm_lm<T>(P, h, grid, s);
+        return;
+    }
     if (h.pdm_lm_head == h.lm_head)
         launch_k(k_gemv<T, EPI_LM, true>, dim3(grid), dim3(TG_THREADS), smem_for(h, EPI_LM), s, h.pdl != 0, P, 0);
     else

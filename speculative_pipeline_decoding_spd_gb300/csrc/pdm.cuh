@@ -39,7 +39,7 @@
 
 namespace spd {
 
-enum { OP_PROJ = 0, OP_QKV, OP_OPROJ, OP_GATEUP, OP_DOWN };
+enum { OP_PROJ = 0, OP_QKV, OP_OPROJ, OP_GATEUP, OP_DOWN, OP_LM };
 
 constexpr int PG_CONSUMERS = 256;              // 8 consumer warps
 constexpr int PG_THREADS = PG_CONSUMERS + 32;  // + 1 producer warp
@@ -63,7 +63,7 @@ __host__ __device__ inline int pg_nch(int kw, int esz) { return (kw * esz + PG_R
 __host__ __device__ inline int pg_kc(int kw, int esz) { return pg_round((kw + pg_nch(kw, esz) - 1) / pg_nch(kw, esz), PG_KB); }
 
 template <int OP> __host__ __device__ inline int pg_N(const Plan &h) {
-    return OP == OP_QKV ? h.qkv_rows : OP == OP_GATEUP ? 2 * h.F : h.d;
+    return OP == OP_QKV ? h.qkv_rows : OP == OP_GATEUP ? 2 * h.F : OP == OP_LM ? h.V : h.d;
 }
 template <int OP> __host__ __device__ inline int pg_K(const Plan &h) {
     return OP == OP_PROJ ? h.nB * h.d : OP == OP_OPROJ ? h.q_rows : OP == OP_DOWN ? h.F : h.d;
@@ -112,8 +112,8 @@ __device__ __forceinline__ PgRows<T, OP> pg_rows(const Plan *__restrict__ P, int
     r.qk_groups = (P->q_rows + P->kv_rows) / 8;
     r.b1 = r.b2 = 0x7fffffff;
     r.p1 = r.p2 = nullptr;
-    if (OP == OP_PROJ) {
-        r.p0 = reinterpret_cast<const T *>(P->proj);
+    if (OP == OP_PROJ || OP == OP_LM) {
+        r.p0 = reinterpret_cast<const T *>(OP == OP_PROJ ? P->proj : P->lm_head);
         return r;
     }
     const LayerW &w = P->pl[layer];
@@ -228,12 +228,13 @@ __device__ __forceinline__ float2 pg_prefetch(const Plan *__restrict__ P, const 
             const int pos = pr.pos0 + xr, hd = P->hd, half = hd >> 1, i = row % hd;
             r = P->rope[(long long)pos * half + (wr < 4 ? i : i - half)];
         }
-    } else if (OP != OP_GATEUP) {
+    } else if (OP == OP_PROJ || OP == OP_OPROJ || OP == OP_DOWN) {
         if (OP != OP_PROJ) r.x = P->Xp[(long long)xr * P->d + row];
         if (sizeof(T) == 2) {
+            // next normalisation: the next GEMM's, after the last layer the LM head's
             const float *gn = OP == OP_PROJ ? P->pl[0].g1 : OP == OP_OPROJ ? P->pl[layer].g2
-                            : layer + 1 < P->Ls ? P->pl[layer + 1].g1 : nullptr;
-            if (gn) r.y = gn[row];
+                            : layer + 1 < P->Ls ? P->pl[layer + 1].g1 : P->pdm_gf;
+            r.y = gn[row];
         }
     }
     return r;
@@ -278,10 +279,12 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
         if (valid) {
             o = OP == OP_PROJ ? v : pre.x + v;
             P->Xp[(long long)xr * P->d + row] = o;
-            // bf16 input row of the next GEMM: x * g of its normalisation (none after the last
-            // layer: the LM head normalises Xp itself)
-            if (sizeof(T) == 2 && (OP != OP_DOWN || layer + 1 < P->Ls))
-                P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * pre.y);
+            // bf16 input row of the next GEMM: x * g of its normalisation; after the last layer
+            // the newest row is the LM head's second input row
+            if (sizeof(T) == 2) {
+                if (OP != OP_DOWN || layer + 1 < P->Ls) P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * pre.y);
+                else if (xr == pr.R - 1) P->Xlm[P->d + row] = __float2bfloat16_rn(o * pre.y);
+            }
         }
         // sum of squares of the 8 rows of this group for x row xr (lanes differing in thread
         // bits 0, 2, 3 hold its 8 weight rows)
@@ -335,6 +338,123 @@ __device__ __forceinline__ uint4 pg_x8(const Plan *__restrict__ P, const PdmRows
                       *reinterpret_cast<uint32_t *>(&p2), *reinterpret_cast<uint32_t *>(&p3));
 }
 
+// ---- LM head on the same machinery (bf16, tied head): rows 0 and 1 of x are the final
+// normalisation's x * g of the token leaving the last stage and of the draft module's
+// newest row, left as bf16 by the target's last down projection and the draft's last down
+// GEMM; their 1/rms scale the logits.
+
+// 1/rms of the two rows, 0 for an absent row (no token leaves the last stage; no draft
+// module): row 0 from the residual of the last stage's slot (warp 0, lane-strided loads in
+// flight together, then the shuffle tree), row 1 from the draft's per-8-row sums of squares
+// of its newest row (warp 1).
+static __device__ __noinline__ void pg_lm_inv_rms(const Plan *__restrict__ P, const PdmRows &pr, float *inv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, d = P->d;
+    if (warp > 1) return;
+    bool ok;
+    float s = 0.f;
+    if (warp == 0) {
+        const DevState *st = P->st;
+        const int n = P->n, es = ring(st->head, n - 1, n + 1);
+        ok = st->valid[es] != 0;
+        if (ok) {
+            const float4 *x = reinterpret_cast<const float4 *>(P->X + (long long)es * d);
+            const int n4 = d >> 2;
+            for (int c0 = 0; c0 < n4; c0 += 32 * 16) {
+                float4 v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c = c0 + lane + 32 * j;
+                    v[j] = c < n4 ? x[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    s = fmaf(v[j].x, v[j].x, s);
+                    s = fmaf(v[j].y, v[j].y, s);
+                    s = fmaf(v[j].z, v[j].z, s);
+                    s = fmaf(v[j].w, v[j].w, s);
+                }
+            }
+        }
+    } else {
+        const int r = pr.R - 1, ng = d / 8;
+        ok = P->Ls > 0 && r >= 0;
+        if (ok) {
+            const float *sp = P->ssp + (long long)r * ng;
+            for (int c0 = 0; c0 < ng; c0 += 32 * 16) {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c = c0 + lane + 32 * j;
+                    v[j] = c < ng ? sp[c] : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) s += v[j];
+            }
+        }
+    }
+    s = warp_sum(s);
+    if (lane == 0) inv[warp] = ok ? 1.0f / sqrtf(s / (float)d + P->eps) : 0.f;
+}
+
+// Argmax of the two logit rows (lowest id on ties): the CTA's candidates (held by the
+// reduction threads of x rows 0 and 1, one per tile slot) are reduced in slot order, then
+// the last CTA to finish merges the CTAs' results and leaves top / topval in the state.
+static __device__ __noinline__ void pg_lm_argmax(const Plan *__restrict__ P, int xr, int wr, float bv, int bi) {
+    __shared__ float s_lv[2][PG_RG];
+    __shared__ int s_li[2][PG_RG];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 128 && xr < 2) {
+        s_lv[xr][wr] = bv;
+        s_li[xr][wr] = bi;
+    }
+    named_sync(PG_BAR, PG_CONSUMERS);
+    if (tid < 2) {
+        float cv = -INFINITY;
+        int ci = 0x7fffffff;
+        for (int w = 0; w < PG_RG; ++w)
+            if (s_lv[tid][w] > cv || (s_lv[tid][w] == cv && s_li[tid][w] < ci)) {
+                cv = s_lv[tid][w];
+                ci = s_li[tid][w];
+            }
+        P->lm_part[blockIdx.x * 4 + tid * 2] = cv;
+        P->lm_part[blockIdx.x * 4 + tid * 2 + 1] = __int_as_float(ci);
+    }
+    __threadfence();
+    named_sync(PG_BAR, PG_CONSUMERS);
+    if (tid == 0) s_last = atomicAdd(P->lm_cnt, 1) == (int)gridDim.x - 1;
+    named_sync(PG_BAR, PG_CONSUMERS);
+    if (!s_last) return;
+    __threadfence();
+    if (warp < 2) {
+        const int row = warp;
+        float cv = -INFINITY;
+        int ci = 0x7fffffff;
+        for (int c = lane; c < (int)gridDim.x; c += 32) {
+            const float v = __ldcg(P->lm_part + c * 4 + row * 2);
+            const int id = __float_as_int(__ldcg(P->lm_part + c * 4 + row * 2 + 1));
+            if (v > cv || (v == cv && id < ci)) {
+                cv = v;
+                ci = id;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, cv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, ci, o);
+            if (ov > cv || (ov == cv && oi < ci)) {
+                cv = ov;
+                ci = oi;
+            }
+        }
+        if (lane == 0) {
+            P->st->top[row] = ci;
+            P->st->topval[row] = cv;
+        }
+    }
+    if (tid == 0) *P->lm_cnt = 0;
+}
+
 // One CTA's share of a draft GEMM: CTA p of m_pdm (row block p / ns, K slab p % ns).
 // smem: the dynamic shared memory; full/empty: PG_MAXNS mbarriers each, initialised (full
 // count 1, empty count 8) and fenced by the caller, like xbar (count 1: the bf16 x rows'
@@ -349,8 +469,9 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     const int ns = P->pdm_ns[OP], kx = P->pdm_kx[OP];
     const int N = pg_N<OP>(*P), K = pg_K<OP>(*P), G8 = N / 8;
     const int nb = m_pdm / ns, b = p / ns, sl = p - (p / ns) * ns;
-    if (b >= nb || pr.R < 1) return;
-    const int R = pr.R;
+    if (b >= nb || (OP != OP_LM && pr.R < 1)) return;
+    // LM head: row 0 = the token leaving the last stage, row 1 = the draft module's newest row
+    const int R = OP == OP_LM ? 2 : pr.R;
     const int k0 = sl * kx, kw = min(kx, K - k0);
     const int gb0 = (int)((long long)G8 * b / nb), gb1 = (int)((long long)G8 * (b + 1) / nb);
     const int nch = pg_nch(kw, ESZ), KC = pg_kc(kw, ESZ);
@@ -361,7 +482,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // global memory already, copied whole into x by bulk copies; the register-resident
     // fragments are then read from there
     constexpr bool BULK = ESZ == 2 && OP != OP_PROJ;
-    const int xbytes = xreg && !BULK ? 0 : pg_xbytes(P->n + 1, kx, ESZ);
+    const int xbytes = xreg && !BULK ? 0 : pg_xbytes(OP == OP_LM ? 2 : P->n + 1, kx, ESZ);
     unsigned char *xs = smem;
     float4 *red = reinterpret_cast<float4 *>(smem + xbytes);
     unsigned char *stages = smem + xbytes + pg_redbytes(MT);
@@ -397,7 +518,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     pdl_trigger();
     if constexpr (BULK) {
         if (tid == 0) {
-            const __nv_bfloat16 *src = OP == OP_OPROJ ? P->ATTb : OP == OP_DOWN ? P->GUb : P->Xb;
+            const __nv_bfloat16 *src = OP == OP_OPROJ ? P->ATTb : OP == OP_DOWN ? P->GUb : OP == OP_LM ? P->Xlm : P->Xb;
             const uint32_t rb = (uint32_t)kw * 2;
             fence_proxy_async();
             mbar_expect_tx(xbar, rb * R);
@@ -408,6 +529,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     }
     // the rows' 1/rms (read by the epilogue, after the first group's barrier at the latest)
     if (OP == OP_QKV || OP == OP_GATEUP) pg_row_inv_rms(P, R, s_inv);
+    if (OP == OP_LM) pg_lm_inv_rms(P, pr, s_inv);
     if constexpr (BULK) {
         if (!mbar_wait(xbar, 0)) P->st->error = ERR_TIMEOUT;
     } else if (!xreg) {
@@ -441,6 +563,11 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     const int gq = lane >> 2, tq = lane & 3;
     uint32_t tile = 0;
     int buf = 0;
+    // LM head: this thread's argmax candidate and the draft row's logits for sampling
+    float lbv = -INFINITY;
+    int lbi = 0x7fffffff;
+    float *dl = nullptr;
+    if (OP == OP_LM && P->temperature > 0.f) dl = P->dlogits + (long long)ring(P->st->head + 1, 0, P->n + 1) * P->V;
     for (int g = gb0; g < gb1; ++g) {
         float2 pre = make_float2(0.f, 0.f);
         if (ns == 1 && tid < 128 * MT) pre = pg_prefetch<T, OP>(P, pr, layer, xr_t, wrows.row_of(g, wr_t), wr_t, xr_t < R);
@@ -551,10 +678,27 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
 #pragma unroll
             for (int w = 0; w < PG_CONSUMERS / 32; ++w) s += rf[(((buf * (PG_CONSUMERS / 32) + w) * MT + rm) * 32 + rl) * 4 + rreg];
             const int row = wrows.row_of(g, wr_t);
-            if (ns == 1) pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R, s_inv, pre);
-            else if (xr_t < R) part[((long long)sl * (P->n + 1) + xr_t) * N + row] = s;
+            if constexpr (OP == OP_LM) {
+                if (xr_t < 2) {
+                    const float z = s * s_inv[xr_t];
+                    P->logits[(long long)xr_t * N + row] = z;
+                    if (xr_t == 1 && dl) dl[row] = z;
+                    if (z > lbv || (z == lbv && row < lbi)) {
+                        lbv = z;
+                        lbi = row;
+                    }
+                }
+            } else if (ns == 1) {
+                pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R, s_inv, pre);
+            } else if (xr_t < R) {
+                part[((long long)sl * (P->n + 1) + xr_t) * N + row] = s;
+            }
         }
         buf ^= 1;
+    }
+    if constexpr (OP == OP_LM) {
+        pg_lm_argmax(P, xr_t, wr_t, lbv, lbi);
+        return;
     }
     if (ns == 1) return;
 
