@@ -130,6 +130,7 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.ATTb = b.take<__nv_bfloat16>((size_t)ns * qr);
     h.GUb = b.take<__nv_bfloat16>((size_t)ns * d->F);
     h.Xlm = b.take<__nv_bfloat16>((size_t)2 * d->d);
+    h.ANCHb = b.take<__nv_bfloat16>((size_t)ns * c->n_anchors * d->d);
     h.ssp = b.take<float>((size_t)MAXS * (d->d / 8));
     {
         // draft GEMM K-slab partials: largest slabs x rows x outputs over the five GEMMs

@@ -95,6 +95,7 @@ struct Plan {
     __nv_bfloat16 *Xb;             // [n+1][d] Xp * g of the next normalisation (1/rms applied after the GEMM)
     __nv_bfloat16 *ATTb;           // [n+1][Hq hd] attention output
     __nv_bfloat16 *GUb;            // [n+1][F] SiLU(gate) * up
+    __nv_bfloat16 *ANCHb;          // [n+1][nB][d] the anchor states as bf16 (the draft projection's input)
     __nv_bfloat16 *Xlm;            // [2][d] LM head rows: x * g_final of the exiting token and of the draft's newest row
     float *pdm_part;               // draft GEMM K-slab partials [slab][n+1][N]
     int *pdm_cnt;                  // draft GEMM row-block arrival counters (zero between launches)

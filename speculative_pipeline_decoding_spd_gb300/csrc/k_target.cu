@@ -594,7 +594,10 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                     const float xn = xold + acc0;
                     P->X[(long long)slot * d + unit] = xn;
                     const int a = P->aidx[layer + 1];
-                    if (a >= 0) P->ANCH[((long long)slot * P->nB + a) * d + unit] = xn;
+                    if (a >= 0) {
+                        P->ANCH[((long long)slot * P->nB + a) * d + unit] = xn;
+                        if (sizeof(T) == 2) P->ANCHb[((long long)slot * P->nB + a) * d + unit] = __float2bfloat16_rn(xn);
+                    }
                     if (lm_row) P->Xlm[unit] = __float2bfloat16_rn(xn * gfin);
                 } else {
                     // logits: tied -> both rows of this vocab id; untied -> row (q >= 4) only

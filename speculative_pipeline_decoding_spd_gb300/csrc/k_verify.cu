@@ -89,10 +89,12 @@ __device__ void embed_into_slot(const Plan *__restrict__ P, int slot, int tok) {
     const T *e = reinterpret_cast<const T *>(P->embed) + (long long)tok * d;
     float *x = P->X + (long long)slot * d;
     float *a0 = P->ANCH + (long long)slot * P->nB * d;
+    __nv_bfloat16 *b0 = P->ANCHb + (long long)slot * P->nB * d;
     for (int k = threadIdx.x; k < d; k += blockDim.x) {
         const float v = WTraits<T>::get(e, k);
         x[k] = v;
         a0[k] = v;
+        if (sizeof(T) == 2) b0[k] = __float2bfloat16_rn(v);
     }
 }
 

@@ -478,10 +478,10 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     const int xpitch = pg_pitch(kx, ESZ);
     const int rowb = pg_pitch(KC, ESZ), stage_bytes = PG_RG * rowb;
     const bool xreg = pg_xreg(MT, ESZ, K, ns);
-    // bf16 weights: the inputs (except the projection's masked anchors) are bf16 rows in
-    // global memory already, copied whole into x by bulk copies; the register-resident
-    // fragments are then read from there
-    constexpr bool BULK = ESZ == 2 && OP != OP_PROJ;
+    // bf16 weights: the inputs are bf16 rows in global memory already, copied whole into x by
+    // bulk copies (the projection's per anchor, masked ones zeroed instead); the
+    // register-resident fragments are then read from there
+    constexpr bool BULK = ESZ == 2;
     const int xbytes = xreg && !BULK ? 0 : pg_xbytes(OP == OP_LM ? 2 : P->n + 1, kx, ESZ);
     unsigned char *xs = smem;
     float4 *red = reinterpret_cast<float4 *>(smem + xbytes);
@@ -516,7 +516,33 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // ------------------------------ consumers -------------------------------------------
     pdl_wait();   // x, its statistics and the counters belong to the preceding launch
     pdl_trigger();
-    if constexpr (BULK) {
+    if constexpr (BULK && OP == OP_PROJ) {
+        // row r, anchor a: the piece [max(k0, a d), min(k0 + kw, (a + 1) d)) of the slab
+        const int d = P->d, a0 = k0 / d, a1 = (k0 + kw - 1) / d;
+        if (tid == 0) {
+            uint32_t tot = 0;
+            for (int r = 0; r < R; ++r)
+                for (int a = a0; a <= a1; ++a)
+                    if (P->anchors[a] <= pr.depth[r]) tot += (uint32_t)(min(k0 + kw, (a + 1) * d) - max(k0, a * d)) * 2;
+            fence_proxy_async();
+            mbar_expect_tx(xbar, tot);
+            for (int r = 0; r < R; ++r)
+                for (int a = a0; a <= a1; ++a) {
+                    if (P->anchors[a] > pr.depth[r]) continue;
+                    const int ka = max(k0, a * d), kb = min(k0 + kw, (a + 1) * d);
+                    bulk_g2s(xs + r * xpitch + (ka - k0) * 2, P->ANCHb + ((long long)pr.slot[r] * P->nB + a) * d + (ka - a * d),
+                             (uint32_t)(kb - ka) * 2, xbar);
+                }
+        }
+        // anchors deeper than the row's token enter as zeros
+        for (int r = 0; r < R; ++r)
+            for (int a = a0; a <= a1; ++a) {
+                if (P->anchors[a] <= pr.depth[r]) continue;
+                const int ka = max(k0, a * d), kb = min(k0 + kw, (a + 1) * d);
+                for (int e = ka + 8 * tid; e < kb; e += 8 * PG_CONSUMERS)
+                    *reinterpret_cast<uint4 *>(xs + r * xpitch + (e - k0) * 2) = make_uint4(0u, 0u, 0u, 0u);
+            }
+    } else if constexpr (BULK) {
         if (tid == 0) {
             const __nv_bfloat16 *src = OP == OP_OPROJ ? P->ATTb : OP == OP_DOWN ? P->GUb : OP == OP_LM ? P->Xlm : P->Xb;
             const uint32_t rb = (uint32_t)kw * 2;
@@ -532,6 +558,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     if (OP == OP_LM) pg_lm_inv_rms(P, pr, s_inv);
     if constexpr (BULK) {
         if (!mbar_wait(xbar, 0)) P->st->error = ERR_TIMEOUT;
+        if (OP == OP_PROJ) named_sync(PG_BAR, PG_CONSUMERS);   // the zeroed pieces
     } else if (!xreg) {
         named_sync(PG_BAR, PG_CONSUMERS);
     }
