@@ -1,9 +1,10 @@
-// Draft-module kernels and the draft GEMM plan.
+// Draft-module kernels, the draft GEMM plan, and the tensor-core LM head.
 //
 // The draft module runs on a second stream, concurrent with the target's rounds: one
 // launch per GEMM (one CTA per SM, the CTA code in pdm.cuh) and one per attention
 // (k_attn.cu).  Its rows' inputs are the step's input states, so nothing in it waits for
-// the target's rounds of the same step; the LM head waits for both streams.
+// the target's rounds of the same step; the LM head waits for both streams.  With bf16
+// weights and a tied head the LM head is the same GEMM over two rows (OP_LM).
 #include "pdm.cuh"
 
 namespace spd {
