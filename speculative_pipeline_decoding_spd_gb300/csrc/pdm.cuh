@@ -297,45 +297,11 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
 }
 
 // Register-resident x: when one 16-row mma tile covers the rows, the whole K of the GEMM is
-// one piece of a tile and each warp's K blocks are at most PG_XRB, every warp keeps the A
-// fragments of its blocks in registers for the whole launch (the same K blocks meet every
-// tile), and the x rows take no shared memory.
+// one piece of a tile and each warp's K blocks are at most PG_XRB, every warp loads the A
+// fragments of its blocks from the staged x once and keeps them in registers for the whole
+// launch (the same K blocks meet every tile).
 __host__ __device__ inline bool pg_xreg(int MT, int esz, int K, int ns) {
     return MT == 1 && esz == 2 && ns == 1 && K * esz <= PG_ROWB && K <= 8 * PG_XRB * PG_KB;
-}
-
-// 8 consecutive x values of row r at GEMM column k (k % 8 == 0), packed as bf16 pairs
-// (normalised inputs as x * g, like the staging).
-template <int OP>
-__device__ __forceinline__ uint4 pg_x8(const Plan *__restrict__ P, const PdmRows &pr, int layer, int r, int k) {
-    const int d = P->d;
-    float4 a, b;
-    if (OP == OP_PROJ) {
-        const int an = k / d, off = k - an * d;
-        const float4 *src = reinterpret_cast<const float4 *>(P->ANCH + ((long long)pr.slot[r] * P->nB + an) * d + off);
-        a = src[0];
-        b = src[1];
-        if (P->anchors[an] > pr.depth[r]) a = b = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else if (OP == OP_QKV || OP == OP_GATEUP) {
-        const float *g = OP == OP_QKV ? P->pl[layer].g1 : P->pl[layer].g2;
-        const float4 *src = reinterpret_cast<const float4 *>(P->Xp + (long long)r * d + k);
-        const float4 x0 = src[0], x1 = src[1];
-        const float4 g0 = *reinterpret_cast<const float4 *>(g + k), g1 = *reinterpret_cast<const float4 *>(g + k + 4);
-        a = make_float4(x0.x * g0.x, x0.y * g0.y, x0.z * g0.z, x0.w * g0.w);
-        b = make_float4(x1.x * g1.x, x1.y * g1.y, x1.z * g1.z, x1.w * g1.w);
-    } else if (OP == OP_OPROJ) {
-        const float4 *src = reinterpret_cast<const float4 *>(P->ATTp + (long long)r * P->q_rows + k);
-        a = src[0];
-        b = src[1];
-    } else {
-        const float4 *src = reinterpret_cast<const float4 *>(P->GUp + (long long)r * P->F + k);
-        a = src[0];
-        b = src[1];
-    }
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
-    __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
-    return make_uint4(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1),
-                      *reinterpret_cast<uint32_t *>(&p2), *reinterpret_cast<uint32_t *>(&p3));
 }
 
 // ---- LM head on the same machinery (bf16, tied head): rows 0 and 1 of x are the final
@@ -482,7 +448,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // bulk copies (the projection's per anchor, masked ones zeroed instead); the
     // register-resident fragments are then read from there
     constexpr bool BULK = ESZ == 2;
-    const int xbytes = xreg && !BULK ? 0 : pg_xbytes(OP == OP_LM ? 2 : P->n + 1, kx, ESZ);
+    const int xbytes = pg_xbytes(OP == OP_LM ? 2 : P->n + 1, kx, ESZ);
     unsigned char *xs = smem;
     float4 *red = reinterpret_cast<float4 *>(smem + xbytes);
     unsigned char *stages = smem + xbytes + pg_redbytes(MT);
@@ -572,13 +538,8 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
 #pragma unroll
             for (int j = 0; j < PG_XRB; ++j) {
                 const int bb = warp + 8 * j, kl = bb * PG_KB + 8 * tq;
-                if constexpr (BULK) {
-                    xf[j][0] = bb < nblk && gq < R ? lds128(xs + gq * xpitch + kl * 2) : z;
-                    xf[j][1] = bb < nblk && gq + 8 < R ? lds128(xs + (gq + 8) * xpitch + kl * 2) : z;
-                } else {
-                    xf[j][0] = bb < nblk && gq < R ? pg_x8<OP>(P, pr, layer, gq, k0 + kl) : z;
-                    xf[j][1] = bb < nblk && gq + 8 < R ? pg_x8<OP>(P, pr, layer, gq + 8, k0 + kl) : z;
-                }
+                xf[j][0] = bb < nblk && gq < R ? lds128(xs + gq * xpitch + kl * 2) : z;
+                xf[j][1] = bb < nblk && gq + 8 < R ? lds128(xs + (gq + 8) * xpitch + kl * 2) : z;
             }
         }
     }
