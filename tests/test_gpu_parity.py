@@ -142,3 +142,35 @@ def test_step_by_step_state_matches_oracle_hidden_states():
             err = np.max(np.abs(X[idx[0]] - ref)) / max(1.0, np.max(np.abs(ref)))
             assert err <= case.tol, (k, s, err)
     e.close()
+
+
+# bf16 with a vocabulary that is not a multiple of 8: the LM head runs as the grouped GEMV
+# (ragged last tile group) instead of the tensor-core GEMM
+RAGGEDV = Case(si.ModelDims(L=6, d=256, Hq=4, Hkv=2, hd=64, F=512, V=2001), n=3, anchors=(0, 3, 6), Ls=2,
+               prompt_len=120, max_new=40, norms="perturbed")
+
+
+def test_ragged_vocab_replay():
+    toks, tr, st, pf = run_gpu(RAGGEDV)
+    o, rep = replay_oracle(RAGGEDV, tr, toks)
+    compare(RAGGEDV, tr, o, rep)
+    assert o.tokens[RAGGEDV.prompt_len:] == toks
+
+
+def test_untied_head_copy_replay():
+    """The draft module's LM head given as a separate copy of the target's: the library takes
+    the untied path (the grouped GEMV with one head per row), and the results still follow the
+    oracle, whose head is the target's."""
+    from speculative_pipeline_decoding_spd_gb300.engine import Engine
+    case = SMALL
+    tg, pd, prompt, m, dtg, dpd = materialise(case)
+    dpd2 = dict(dpd)
+    dpd2["lm_head"] = dtg["lm_head"].clone()
+    e = Engine(case.dm, dtg, dpd2, case.n, case.anchors, max_seq=case.max_seq, max_new=case.max_new)
+    out, cnt, _ = e.generate(torch.from_numpy(prompt).cuda())
+    toks = out[:cnt].cpu().tolist()
+    tr = e.trace()
+    e.close()
+    o, rep = replay_oracle(case, tr, toks)
+    compare(case, tr, o, rep)
+    assert o.tokens[case.prompt_len:] == toks
