@@ -32,6 +32,9 @@ WIDE = Case(si.ModelDims(L=32, d=256, Hq=4, Hkv=2, hd=64, F=512, V=1500), n=16, 
 # happen in the slab-finishing pass), down three
 WIDEK = Case(si.ModelDims(L=32, d=2560, Hq=8, Hkv=2, hd=128, F=2560, V=1000), n=16, anchors=(0, 16, 32), Ls=1,
              prompt_len=40, max_new=40, norms="perturbed")
+# bf16, 2 stages of 3 layers with 2 draft layers (more draft layers relative to the stages)
+INROUNDS = Case(si.ModelDims(L=6, d=512, Hq=8, Hkv=2, hd=64, F=1024, V=1600), n=2, anchors=(0, 3, 6), Ls=2,
+                prompt_len=200, max_new=48, norms="perturbed")
 # MULTI's draft projection (K = 5 x 2560) is split into K slabs across CTAs; its QKV, O, gate/up
 # and down keep x in registers (one 16-row tile, K <= 2560); WIDE's 17 rows keep x in shared memory.
 
@@ -53,7 +56,8 @@ def test_prefill_logits(case):
     _prefill_logits_close(case, pf)
 
 
-@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI, WIDE, WIDEK], ids=["tiny", "small", "hd128", "multi", "wide", "widek"])
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI, WIDE, WIDEK, INROUNDS],
+                         ids=["tiny", "small", "hd128", "multi", "wide", "widek", "inrounds"])
 def test_greedy_draft_module_replay(case):
     toks, tr, st, pf = run_gpu(case)
     o, rep = replay_oracle(case, tr, toks)
@@ -62,8 +66,9 @@ def test_greedy_draft_module_replay(case):
     assert st["N"] == case.max_new - 1 and st["K"] == len(tr)
 
 
-@pytest.mark.parametrize("case,p", [(TINY, 0.6), (SMALL, 0.5), (SMALL, 0.9), (HD128, 0.7), (MULTI, 0.6), (WIDE, 0.8)],
-                         ids=["tiny-0.6", "small-0.5", "small-0.9", "hd128-0.7", "multi-0.6", "wide-0.8"])
+@pytest.mark.parametrize("case,p", [(TINY, 0.6), (SMALL, 0.5), (SMALL, 0.9), (HD128, 0.7), (MULTI, 0.6), (WIDE, 0.8),
+                                    (INROUNDS, 0.7)],
+                         ids=["tiny-0.6", "small-0.5", "small-0.9", "hd128-0.7", "multi-0.6", "wide-0.8", "inrounds-0.7"])
 def test_forced_draft_replay(case, p):
     ar = ar_reference(case)
     tg, pd, prompt, m, _, _ = materialise(case)
