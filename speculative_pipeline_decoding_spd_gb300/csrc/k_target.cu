@@ -1,6 +1,5 @@
 // Target-model kernels of one pipeline step: the grouped per-stage GEMVs and the
-// batched LM head (the latter here for fp32 weights or an untied head; a tied bf16 head
-// runs as a tensor-core GEMM, k_pdm.cu).
+// batched LM head.
 //
 // Speculative pipeline decoding (abstract; machine review "The reading"): the target is
 // cut into n stages and the n in-flight tokens advance through their own stage in the
