@@ -12,10 +12,12 @@
 // does one GEMM; per CTA:
 //   * a producer warp streams 8-row tiles of W (each row piece up to 6 KB, 1-D bulk
 //     copies) into a shared-memory ring signalled by mbarriers;
-//   * the consumer warps stage the R rows of x for the CTA's K slab in shared memory as bf16
-//     (fp32 for fp32 weights), with the norm weight / anchor masking fused into the staging;
-//     an RMS-normalised input is staged as x * g and its row's 1/rms (a per-row scalar)
-//     scales the GEMM's output instead, so staging does not wait for the row statistics;
+//   * the R rows of x for the CTA's K slab go to shared memory: for bf16 weights the kernel
+//     before left them as bf16 rows in global memory and one thread copies them with bulk
+//     copies (the projection per anchor, deeper anchors zeroed); for fp32 weights the
+//     consumer warps load and stage them with the norm weight / anchor masking fused in.
+//     An RMS-normalised input is x * g, and its row's 1/rms (a per-row scalar) scales the
+//     GEMM's output instead, so staging does not wait for the row statistics;
 //   * the 8 consumer warps split each tile's K range into 32-element blocks (block b to
 //     warp b mod 8); per block a warp runs two m16n8k16 tensor-core steps with the x rows
 //     as the 16-row A operand and the 8 weight rows as the B operand, both taking K in the
