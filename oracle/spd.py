@@ -6,12 +6,14 @@ Method (speculative pipeline decoding; page 1 abstract; page 2 "The reading",
 "What carries the argument", "Core claim", referee comments on sections 3.3, 3.4 and
 4.2 Eq. 9, and section 3.5 on rejection sampling):
   * the L target layers are cut into n stages; stage s holds layers [b_s, b_{s+1}),
-    b_s = floor(s L / n) (uniform split; the paper's non-uniform split is not used);
+    b_s = floor(s L / n) (uniform split), or an explicit non-uniform partition;
   * n in-flight tokens of ONE sequence occupy the stages, the token in stage s sitting
     one position behind the token in stage s-1; one step runs every occupied stage on
     its own token, then shifts all tokens one stage deeper;
   * concurrently, the draft module reads the step's INPUT states (early-start
-    schedule) and proposes the token after the newest one; it enters stage 0;
+    schedule) and proposes the token after the newest one; it enters stage 0 (the
+    ablated alternative, also simulated: the module runs after the step on its OUTPUT
+    states);
   * when a token leaves the last stage its target prediction verifies the draft one
     position later (streaming verification, one check per step); on a mismatch the KV
     cache is truncated after the exiting token, every in-flight token is dropped and
@@ -41,11 +43,21 @@ from .model import KVCache, Model, argmax_fp32
 from .sampling import inverse_cdf, keep, probs, residual
 
 
-def stage_bounds(L: int, n: int) -> List[int]:
-    """b_s = floor(s L / n), s = 0..n (stage s holds layers [b_s, b_{s+1}))."""
+def stage_bounds(L: int, n: int, bounds: Optional[Sequence[int]] = None) -> List[int]:
+    """Stage s holds layers [b_s, b_{s+1}), s = 0..n-1.
+
+    Uniform split (the pages speak of L/n layers per stage): b_s = floor(s L / n).
+    ``bounds`` gives a non-uniform partition instead (page 2, referee report, minor
+    comment on Appendix C.1: concrete non-uniform layer assignments, not yet tried in the
+    paper): n + 1 integers 0 = b_0 < b_1 < ... < b_n = L, every stage non-empty."""
     if not (1 <= n <= L):
         raise ValueError("need 1 <= n <= L")
-    return [(s * L) // n for s in range(n + 1)]
+    if bounds is None:
+        return [(s * L) // n for s in range(n + 1)]
+    b = [int(x) for x in bounds]
+    if len(b) != n + 1 or b[0] != 0 or b[-1] != L or any(b[i + 1] <= b[i] for i in range(n)):
+        raise ValueError("stage bounds must be 0 = b_0 < b_1 < ... < b_n = L")
+    return b
 
 
 def closed_form_alpha(n: int, p: float) -> float:
@@ -99,11 +111,14 @@ class Replay:
         if other == mine:
             return mine
         c = np.cumsum(w) / np.sum(w)
-        lo, hi = min(mine, other), max(mine, other)
-        # the boundary between the two picks is c[lo]..c[hi-1]; u must sit within tol_u of it
-        if c[lo] - self.tol_u <= u <= c[hi - 1] + self.tol_u:
-            self.adopted += 1
-            return int(other)
+        # the other pick owns the interval [c[other-1], c[other]) of the unit line; it is
+        # adopted only when u lies within tol_u of that interval (a draw that moved across
+        # one boundary because the two sides' cumulative sums differ by rounding)
+        if 0 <= other < len(w) and w[other] > 0.0:
+            lo = c[other - 1] if other > 0 else 0.0
+            if lo - self.tol_u <= u < c[other] + self.tol_u:
+                self.adopted += 1
+                return int(other)
         self.mismatches.append((t, what, mine, int(other), float(u)))
         return mine
 
@@ -152,14 +167,21 @@ class SPDOracle:
     def __init__(self, model: Model, n: int, max_seq: int, temperature: float = 0.0, seed: int = 2,
                  forced_p: Optional[float] = None, forced_ref: Optional[Sequence[int]] = None,
                  replay: Optional[Replay] = None, track: bool = False,
-                 accept_script: Optional[Sequence[int]] = None):
+                 accept_script: Optional[Sequence[int]] = None, bounds: Optional[Sequence[int]] = None,
+                 speculate: str = "input"):
         dm = model.dm
         # schedule checks only: a list of keep decisions consumed one per verification,
         # overriding the token comparison (the committed token is then the draft or the
         # target's token as the decision says)
         self.script = None if accept_script is None else list(accept_script)
         self.m, self.n, self.T, self.seed = model, n, float(temperature), int(seed)
-        self.b = stage_bounds(dm.L, n)
+        self.b = stage_bounds(dm.L, n, bounds)
+        if speculate not in ("input", "output"):
+            raise ValueError("speculate must be 'input' or 'output'")
+        # "input": the draft module reads the step's input states, concurrently with the
+        # step (the paper's early-start schedule); "output": it runs after the step on its
+        # output states (the ablation the referee report lists)
+        self.speculate = speculate
         if forced_p is not None and forced_ref is None:
             raise ValueError("forced drafts need the reference stream")
         self.forced_p, self.ref = forced_p, (None if forced_ref is None else np.asarray(forced_ref))
@@ -235,36 +257,60 @@ class SPDOracle:
             return self.replay.pick_sample(pD, u0, other, "draft", self.t), pD
         return inverse_cdf(pD, u0), pD
 
+    def _draft_rows(self) -> List[tuple]:
+        """(token, depth) rows of the draft module in this step, oldest position first.
+
+        Input-state schedule (before the step's target work): the token that left the
+        pipeline in the previous step, at full depth L (its K,V join the module's cache
+        for good), then the in-flight tokens from the deepest stage to stage 0 at their
+        stages' input depths b_s.  Output-state schedule (after the target work): the
+        in-flight tokens at their output depths b_{s+1}; the one leaving the last stage
+        is then at depth L and joins the cache."""
+        n, b, L = self.n, self.b, self.m.dm.L
+        rows = []
+        if self.speculate == "input":
+            if self.pending is not None:
+                rows.append((self.pending, L))
+            for s in range(n - 1, -1, -1):
+                if self.slots[s] is not None:
+                    rows.append((self.slots[s], b[s]))
+        else:
+            for s in range(n - 1, -1, -1):
+                if self.slots[s] is not None:
+                    rows.append((self.slots[s], b[s + 1]))
+        for i in range(1, len(rows)):
+            assert rows[i][0].pos == rows[i - 1][0].pos + 1, "draft-module rows must be consecutive"
+        return rows
+
+    def _run_draft_module(self, rows, rep, t):
+        """Project the rows' masked anchor features, run the draft layers over their
+        positions (causal over the cached prefix and the block), final norm, LM head.
+        Returns (logits of the newest row, its argmax under the replay rule)."""
+        m = self.m
+        feats = np.stack([m.feature(tk.anchors, dep) for (tk, dep) in rows])
+        Hp = m.pdm_block(feats, rows[0][0].pos, self.pkv)
+        zD = m.pdm_logits(Hp[-1])
+        if self.replay is not None and self.forced_p is None and self.T == 0.0:
+            top = self.replay.pick_argmax(zD, None if rep is None else rep.get("pdm_top"), "pdm", t)
+        else:
+            top = argmax_fp32(zD)
+        return zD, top
+
     def step(self) -> dict:
         m, n, b = self.m, self.n, self.b
         self.t += 1
         t = self.t
         rep = None if self.replay is None else self.replay.steps.get(t)
-        # ---- draft module on the step's input states ---------------------------------
-        rows = []
-        if self.pending is not None:
-            rows.append((self.pending, m.dm.L))
-        for s in range(n - 1, -1, -1):
-            if self.slots[s] is not None:
-                rows.append((self.slots[s], b[s]))
-        for i in range(1, len(rows)):
-            assert rows[i][0].pos == rows[i - 1][0].pos + 1, "draft-module rows must be consecutive"
-        partial = sum(1 for (tk, dep) in rows if dep < m.dm.L)
-        self.max_inflight_partial = max(self.max_inflight_partial, partial)
         newest = self.slots[0]
         P = newest.pos
         pdm_top = -1
         zD = None
-        if m.pdm_layers:
-            feats = np.stack([m.feature(tk.anchors, dep) for (tk, dep) in rows])
-            Hp = m.pdm_block(feats, rows[0][0].pos, self.pkv)
-            zD = m.pdm_logits(Hp[-1])
-            if self.replay is not None and self.forced_p is None and self.T == 0.0:
-                pdm_top = self.replay.pick_argmax(zD, None if rep is None else rep.get("pdm_top"), "pdm", t)
-            else:
-                pdm_top = argmax_fp32(zD)
-        self.pkv_len = rows[0][0].pos + (1 if self.pending is not None else 0)
-        draft_tok, draft_pD = self._draft(P, zD, pdm_top, rep)
+        rows: List[tuple] = []
+        # ---- input-state schedule: the draft module on the step's input states ------------
+        if self.speculate == "input":
+            rows = self._draft_rows()
+            if m.pdm_layers:
+                zD, pdm_top = self._run_draft_module(rows, rep, t)
         # ---- target: each occupied stage runs its own layers on its own token ---------
         for s in range(n):
             tk = self.slots[s]
@@ -276,15 +322,26 @@ class SPDOracle:
                 for li in range(b[s], b[s + 1]):
                     self.kv.live[li][tk.pos] = True
                 _check_reads(self.kv, reads, t)
+        # ---- output-state schedule: the draft module after the step, on its outputs ---------
+        if self.speculate == "output":
+            rows = self._draft_rows()
+            if m.pdm_layers:
+                zD, pdm_top = self._run_draft_module(rows, rep, t)
+        partial = sum(1 for (tk, dep) in rows if dep < m.dm.L)
+        self.max_inflight_partial = max(self.max_inflight_partial, partial)
+        self.last_zD = zD
+        self.pkv_len = rows[0][0].pos + sum(1 for (tk, dep) in rows if dep == m.dm.L)
+        draft_tok, draft_pD = self._draft(P, zD, pdm_top, rep)
         # ---- streaming verification of the draft one position behind the exiting token
         ex = self.slots[n - 1]
         rec = dict(t=t, exit_pos=-1, draft=-1, target=-1, accept=-1, commit=-1,
                    pdm_top=pdm_top, new_draft=int(draft_tok), pdm_logit=(None if zD is None else float(zD[pdm_top])),
-                   target_logit=None)
+                   target_logit=None, pdm_rows=[(tk.pos, dep) for (tk, dep) in rows])
         flushed = False
         if ex is not None:
             q = ex.pos
             zT = m.logits(ex.H[0])
+            self.last_zT = zT
             if n >= 2:
                 nxt = self.slots[n - 2]
                 x, pD = nxt.tok, nxt.pD
@@ -316,7 +373,9 @@ class SPDOracle:
             self.tokens.append(int(commit))
             self.N += 1
             rec.update(exit_pos=q, draft=int(x), target=int(y), accept=int(ok), commit=int(commit))
-            self.pending = ex
+            # input-state schedule: the exited token is the draft module's full-depth row of
+            # the next step (the output-state schedule took it in this step)
+            self.pending = ex if self.speculate == "input" else None
             if not ok:
                 flushed = True
                 for li in range(m.dm.L):
@@ -335,7 +394,8 @@ class SPDOracle:
         return rec
 
     def fork(self, n: Optional[int] = None, forced_p: Optional[float] = None,
-             forced_ref: Optional[Sequence[int]] = None, replay: Optional[Replay] = None) -> "SPDOracle":
+             forced_ref: Optional[Sequence[int]] = None, replay: Optional[Replay] = None,
+             bounds: Optional[Sequence[int]] = None, speculate: Optional[str] = None) -> "SPDOracle":
         """A copy of this simulator right after its prefill, before the first step, with its
         own stage count, draft rule and replay record: several runs from one prompt pass.
         The model's weights are shared; caches, token list and stage slots are copied."""
@@ -348,7 +408,9 @@ class SPDOracle:
         o = SPDOracle.__new__(SPDOracle)
         o.__dict__.update(self.__dict__)
         o.n = self.n if n is None else n
-        o.b = stage_bounds(self.m.dm.L, o.n)
+        o.b = stage_bounds(self.m.dm.L, o.n, bounds)
+        if speculate is not None:
+            o.speculate = speculate
         o.forced_p, o.ref = forced_p, (None if forced_ref is None else np.asarray(forced_ref))
         o.replay = replay
         for name in ("kv", "pkv"):
@@ -413,13 +475,14 @@ def ar_decode(model: Model, prompt: Sequence[int], max_new: int, max_seq: int,
     return out
 
 
-def replay_decisions(n: int, L: int, prompt_len: int, steps: Sequence[dict]) -> List[dict]:
+def replay_decisions(n: int, L: int, prompt_len: int, steps: Sequence[dict],
+                     bounds: Optional[Sequence[int]] = None) -> List[dict]:
     """Pure state machine of the staircase (no arithmetic): given, per step, the token the
     draft module proposed (``new_draft``) and, when a token exits, the target's choice
     (``target``) and the keep decision (``accept``; derived as draft == target when
     absent), recompute exit positions, commits and the per-layer KV lengths.  Used to
     check another implementation's trace at any size."""
-    b = stage_bounds(L, n)
+    b = stage_bounds(L, n, bounds)
     slots: List[Optional[list]] = [[prompt_len, None]] + [None] * (n - 1)   # [pos, tok]
     length = [prompt_len] * L
     out = []
