@@ -1,11 +1,16 @@
-"""Throughput of the speculative-pipeline-decoding step on the 4B shape (n = 8).
+"""Throughput of the speculative-pipeline-decoding step (default: 4B shape, n = 8, forced p = 0.6).
 
 One bench "step" is one pipeline step: every occupied stage runs its layers on its own
 token, the draft module runs on the second stream, then the LM head and device-side
-verification / rollback.  The timed region is K consecutive steps of a 512-token
-generation after the (untimed) prefill; value = committed tokens / device time.
+verification / rollback.  The timed region is K consecutive steps of a generation after
+the (untimed) prefill; value = committed tokens / device time.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--mode forced-0.6]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--mode forced-0.6 | greedy | t1] [--shape 4b | 8b] [--n N] [--speculate input|output]
+
+Modes: forced-<p> (drafts equal the greedy token with probability p), greedy (the draft
+module's argmax), t1 (the T = 1 workload: 4B shape, prompt 256, rejection sampling).
+Shapes: 4b (L36 d2560, prompt 512) and 8b (L36 d4096, prompt 4096, Ls 2).
 
 Multi-GPU: independent replicas (one sequence per GPU, no collective on the data path);
 value = all ranks' committed tokens / max-over-ranks time.
@@ -33,6 +38,7 @@ import spd_inputs as si  # noqa: E402
 
 METRIC = "committed tokens/s + step us (4B-shape bf16, n=8); weight GB/s vs 8 TB/s HBM"
 WL = si.SHAPE_4B
+NOMINAL_HBM_GBS = 8000.0     # the metric's stated HBM peak
 
 
 def parse():
@@ -41,7 +47,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--mode", default="forced-0.6", help="forced-<p> or greedy (draft-module argmax)")
+    ap.add_argument("--mode", default="forced-0.6", help="forced-<p>, greedy (draft-module argmax) or t1 (T = 1)")
+    ap.add_argument("--shape", default="4b", choices=["4b", "8b"])
+    ap.add_argument("--n", type=int, default=0, help="pipeline stages (default: the workload's)")
+    ap.add_argument("--speculate", default="input", choices=["input", "output"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true", help="profiling runs: leave out the host-buffer leg")
     ap.add_argument("--layers", type=int, default=0,
@@ -51,6 +60,35 @@ def parse():
 
 def mode_p(mode: str):
     return float(mode.split("-", 1)[1]) if mode.startswith("forced-") else None
+
+
+def mode_temperature(mode: str) -> float:
+    return 1.0 if mode == "t1" else 0.0
+
+
+def alpha_ref(mode: str, n: int):
+    """The commit rate both CPU figures convert steps/s with: the closed form for forced
+    drafts (renewal argument: 1 / (1 + (n - 1)(1 - p))), 1/n for greedy drafting by the
+    random-init draft module (its argmax never matches the target's, so every commit
+    takes the n steps of a refill), None at T = 1 (no closed form)."""
+    p = mode_p(mode)
+    if p is not None:
+        return 1.0 if p >= 1.0 else 1.0 / (1.0 + (n - 1) * (1.0 - p))
+    if mode == "greedy":
+        return 1.0 / n
+    return None
+
+
+def select_workload(args) -> si.Workload:
+    """The bench workload: shape and mode select one of the workloads' model sizes."""
+    if args.mode == "t1":
+        wl = si.SHAPE_4B_T1
+    else:
+        wl = si.SHAPE_8B if args.shape == "8b" else si.SHAPE_4B
+    if args.n:
+        wl = si.Workload(wl.name, wl.dims, n=args.n, anchors=wl.anchors, Ls=wl.Ls, prompt_len=wl.prompt_len,
+                         max_new=wl.max_new, temperature=wl.temperature, forced_p=wl.forced_p)
+    return wl
 
 
 def peaks():
@@ -160,8 +198,12 @@ def run_gb300(args, ws, rank, local):
         tg = si.make_target(dm, 0)
         pd = si.make_pdm(dm, WL.Ls, len(WL.anchors), 0)
     prompt = torch.from_numpy(si.make_prompt(dm.V, WL.prompt_len, 1 + rank)).cuda()
+    T = mode_temperature(args.mode)
+    spec = dict(speculate=args.speculate, temperature=T)
     # the generation must outlast warmup + timed steps
     alpha_lo = 1.0 / n if p is None else 1.0 / (1.0 + (n - 1) * (1.0 - p))
+    if T > 0:
+        alpha_lo = 1.0     # sampled drafts are often kept: size for one commit per step
     max_new = max(WL.max_new, int(math.ceil((args.warmup + args.steps + 2 * n) * min(1.0, alpha_lo * 1.3))) + 8)
     max_seq = WL.prompt_len + max_new + n + 8
     forced_ref = None
@@ -174,7 +216,7 @@ def run_gb300(args, ws, rank, local):
     # headline: the step graphs hold no timing events (events between kernels would cut the
     # programmatic launch overlap of the kernels around them)
     e = Engine(dm, tg, pd, n, WL.anchors, max_seq=max_seq, max_new=max_new, seed=2,
-               force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True, timing=False)
+               force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True, timing=False, **spec)
     e.prefill(prompt)
     e.step(args.warmup)
     N0 = e.stats()["N"]
@@ -214,7 +256,7 @@ def run_gb300(args, ws, rank, local):
     # roofline kernel: a second timed region of the same workload whose step graphs record a
     # CUDA event pair around every gate/up launch on its stream (spd_kernel_timing)
     er = Engine(dm, tg, pd, n, WL.anchors, max_seq=max_seq, max_new=max_new, seed=2,
-                force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True, timing=True)
+                force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True, timing=True, **spec)
     er.prefill(prompt)
     er.step(args.warmup)
     t0_ms, l0 = er.kernel_timing()
@@ -240,7 +282,7 @@ def run_gb300(args, ws, rank, local):
                     e2e_steps=1, max_new=max_new, prompt_len=WL.prompt_len,
                     launches_per_step=5 * max(sizes) + 1 + 5 * WL.Ls + 2)
     e2 = Engine(dm, tg, pd, n, WL.anchors, max_seq=WL.prompt_len + WL.max_new + n + 8, max_new=WL.max_new, seed=2,
-                force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True)
+                force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True, **spec)
     host_prompt = prompt.cpu().numpy()
     e2.generate(host_prompt, on_host=True)   # warm
     torch.cuda.synchronize()
@@ -255,28 +297,46 @@ def run_gb300(args, ws, rank, local):
 
 
 # ---------------------------------------------------------------------------------------
-def oracle_sample(n_steps: int, prompt_len: int = 32):
-    """The CPU oracle on the same shape: fp64 model, short prompt (prefill untimed), then
-    n_steps pipeline steps timed on all host cores.  Returns (steps/s, seconds, cores)."""
-    from oracle import Model, SPDOracle
+def oracle_sample(n_steps: int, mode: str, prompt_len: int = 32, e2e: bool = False):
+    """The CPU oracle on the bench workload's shape: fp64 model, a short prompt (prefill
+    untimed) then n_steps pipeline steps timed on all host cores.  With e2e, the workload's
+    own prompt instead, and the prefill timed too.  Returns (steps/s, commits, decode s,
+    prefill s, cores)."""
+    from oracle import Model, SPDOracle, ar_decode
     dm = WL.dims
     tg = si.make_target(dm, 0)
     pd = si.make_pdm(dm, WL.Ls, len(WL.anchors), 0)
     m = Model(dm, tg, pd, WL.anchors)
     del tg, pd
-    prompt = si.make_prompt(dm.V, prompt_len, 1)
-    o = SPDOracle(m, WL.n, prompt_len + n_steps + WL.n + 8)
+    plen = WL.prompt_len if e2e else prompt_len
+    prompt = si.make_prompt(dm.V, plen, 1)
+    p = mode_p(mode)
+    kw = {}
+    if p is not None:
+        # forced drafts follow the oracle's own greedy stream (not timed)
+        ar = ar_decode(m, prompt, n_steps + 2, plen + n_steps + WL.n + 8)
+        kw = dict(forced_p=p, forced_ref=list(prompt) + ar + [0] * (n_steps + WL.n + 8))
+    o = SPDOracle(m, WL.n, plen + n_steps + WL.n + 8, temperature=mode_temperature(mode), seed=2, **kw)
+    t = time.perf_counter()
     o.prefill(prompt)
+    t_pf = time.perf_counter() - t
     t = time.perf_counter()
     for _ in range(n_steps):
         o.step()
     dt = time.perf_counter() - t
-    return n_steps / dt, dt, os.cpu_count()
+    return n_steps / dt, o.N, dt, t_pf, os.cpu_count()
+
+
+def cpu_alpha(mode: str, n: int, measured: float) -> float:
+    """alpha_ref where a closed form exists, else the commit rate the run measured."""
+    a = alpha_ref(mode, n)
+    return measured if a is None else a
 
 
 def main():
     args = parse()
     global WL
+    WL = select_workload(args)
     if args.layers:
         L = args.layers
         WL = si.Workload(f"{WL.name}-L{L}", si.shrink(WL.dims, L=L), n=min(WL.n, L),
@@ -301,9 +361,12 @@ def main():
     if os.path.exists(tp):
         tj = json.load(open(tp))
         src = os.path.join(ROOT, "speculative_pipeline_decoding_spd_gb300", "csrc", "k_target.cu")
-        if tj.get("k_target_sha") == source_hash(src):
+        if tj.get("k_target_sha") == source_hash(src) and tj.get("d") == WL.dims.d and tj.get("F") == WL.dims.F:
             per_stage_layer = tj["dram_bytes_per_stage_layer"]
             traffic = per_stage_layer * (r["gate_bytes"] / (2 * WL.dims.F * WL.dims.d * 2)) / r["gate_launches"]
+    ms_step = ms_max / args.steps
+    a_cf = alpha_ref(args.mode, WL.n) if p is not None else None
+    wgbs = r["wbytes"] / (r["ms"] / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -311,7 +374,7 @@ def main():
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_max / args.steps, 4),
+        "ms_per_step": round(ms_step, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -319,12 +382,18 @@ def main():
         "data": "synthetic (seeded random-init weights drawn on the GPU, uniform-random prompt ids)",
         "config": {"workload": f"{WL.name}: L{WL.dims.L} d{WL.dims.d} {WL.dims.Hq}q/{WL.dims.Hkv}kv x{WL.dims.hd} "
                                f"F{WL.dims.F} V{WL.dims.V}, n={WL.n}, Ls={WL.Ls}, "
-                               f"anchors {','.join(str(a) for a in WL.anchors)}, prompt {WL.prompt_len}, {args.mode}",
+                               f"anchors {','.join(str(a) for a in WL.anchors)}, prompt {WL.prompt_len}, {args.mode}"
+                               + ("" if args.speculate == "input" else ", output-state schedule"),
                    "mode": args.mode, "n": WL.n, "prompt_len": WL.prompt_len, "max_new": r["max_new"],
+                   "speculate": args.speculate,
                    "parallelism": f"replicas x{ws}", "l2": "no flush needed: ~9 GB of weights per step >> 129 MB L2",
                    "alpha": round(r["alpha"], 4), "S0": round(r["alpha"] * WL.n, 3),
-                   "weight_GBps": round(r["wbytes"] / (r["ms"] / 1e3) / 1e9, 1),
-                   "weight_frac_of_hbm": round(r["wbytes"] / (r["ms"] / 1e3) / 1e9 / hbm, 4)},
+                   "tok_s_at_closed_form_alpha": None if a_cf is None else round(a_cf * 1e3 / ms_step, 2),
+                   "closed_form_alpha": None if a_cf is None else round(a_cf, 4),
+                   "weight_GBps": round(wgbs, 1),
+                   "weight_frac_of_measured_hbm": round(wgbs / hbm, 4),
+                   "weight_frac_of_nominal_hbm": round(wgbs / NOMINAL_HBM_GBS, 4),
+                   "hbm_denominators_GBps": {"measured": hbm, "nominal": NOMINAL_HBM_GBS}},
         "roofline": {"kernel": "target gate/up GEMV (k_gemv EPI_GATEUP)", "bound": "hbm",
                      "timed": "CUDA events around each gate/up launch on its stream, in a second timed region of the "
                               "same workload",
@@ -332,20 +401,23 @@ def main():
                      "traffic": None if traffic is None else round(traffic), "peak_kind": f"hbm_gbs ({pk_kind})",
                      "launches": r["gate_launches"]},
         "clocks": r["clocks"],
-        "e2e": {"value": round(r["e2e_tokens"] / r["e2e_s"], 2), "unit": "generated tokens/s (spd_generate, host "
-                "buffers, prefill + decode)", "h2d_bytes_per_step": round(4 * r["prompt_len"] / r["e2e_steps"], 3),
-                "d2h_bytes_per_step": round((4 * WL.max_new + 32 * math.ceil(r["e2e_steps"] / 8)) / r["e2e_steps"], 3)},
+        "e2e": {"value": round(r["e2e_tokens"] / r["e2e_s"], 2), "unit": "generated tokens/s (prefill + decode, "
+                "host buffers)", "h2d_bytes_per_step": round(4 * r["prompt_len"] / r["e2e_steps"], 3),
+                "d2h_bytes_per_step": round((4 * WL.max_new + 32 * math.ceil(r["e2e_steps"] / 8)) / r["e2e_steps"], 3),
+                "call": "spd_generate"},
         "gpu_launches": r["launches_per_step"] * args.steps,
     }
     if ws == 1 and not args.no_cpu_baseline:
         try:
-            sps, dt, cores = oracle_sample(12)
-            alpha = r["alpha"]
+            sps, commits, dt, _, cores = oracle_sample(12, args.mode)
+            alpha = cpu_alpha(args.mode, WL.n, r["alpha"])
             line["cpu_baseline"] = {"value": round(sps * alpha, 4), "unit": "committed tokens/s", "cores": cores,
                                     "kind": "oracle",
-                                    "sample": f"fp64 oracle, same 4B shape n=8, 32-token prompt (prefill untimed), 12 "
-                                              f"pipeline steps timed ({dt:.1f} s); tokens/s = steps/s x alpha {alpha:.3f} "
-                                              f"of the GPU run"}
+                                    "sample": f"fp64 oracle, same shape and mode, n={WL.n}, 32-token prompt (prefill "
+                                              f"untimed), 12 pipeline steps timed ({dt:.1f} s); tokens/s = steps/s x "
+                                              f"alpha {alpha:.4f} ("
+                                              + ("closed form" if alpha_ref(args.mode, WL.n) is not None
+                                                 else "the GPU run's") + ")"}
         except MemoryError as ex:
             line["cpu_baseline"] = {"value": None, "unit": "committed tokens/s", "cores": os.cpu_count(),
                                     "kind": "oracle", "sample": f"not run: {ex}"}
@@ -363,25 +435,34 @@ def _sum_op():
 
 
 def main_reference(args, ws, rank):
-    """The oracle (plain fp64 CPU restatement of the method) on this arm's workload."""
+    """The oracle (plain fp64 CPU restatement of the method) on this arm's workload.  Each
+    timed step is one pipeline step of the oracle; value = steps/s x the same alpha the
+    GPU arm's cpu_baseline uses (closed form where one exists, else the oracle sample's
+    own commit rate).  e2e: the workload's own prompt, prefill and steps timed together."""
     if rank != 0:
         return
     k = max(1, min(args.steps, 12))
     w = max(0, min(args.warmup, 2))
-    from oracle import closed_form_alpha
-    p = mode_p(args.mode)
-    alpha = closed_form_alpha(WL.n, p) if p is not None else 1.0 / WL.n
-    sps, dt, cores = oracle_sample(k + w)
+    sps, commits, dt, _, cores = oracle_sample(k + w, args.mode)
+    alpha = cpu_alpha(args.mode, WL.n, commits / (k + w))
     value = sps * alpha
+    e_sps, e_commits, e_dt, e_pf, _ = oracle_sample(4, args.mode, e2e=True)
+    e2e_tokens = 1 + 4 * alpha
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "committed tokens/s", "n_gpus": 1,
         "steps": k, "warmup": w, "ms_per_step": round(1e3 / sps, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{WL.name}, n=8, {args.mode}", "mode": args.mode},
+        "config": {"workload": f"{WL.name}: L{WL.dims.L} d{WL.dims.d} {WL.dims.Hq}q/{WL.dims.Hkv}kv x{WL.dims.hd} "
+                               f"F{WL.dims.F} V{WL.dims.V}, n={WL.n}, Ls={WL.Ls}, "
+                               f"anchors {','.join(str(a) for a in WL.anchors)}, prompt {WL.prompt_len}, {args.mode}",
+                   "mode": args.mode, "n": WL.n},
         "cpu_baseline": {"value": round(value, 4), "unit": "committed tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"fp64 oracle, 4B shape n=8, 32-token prompt (prefill untimed), {k + w} steps "
-                                   f"({dt:.1f} s); tokens/s = steps/s x closed-form alpha {alpha:.3f}"},
-        "e2e": {"value": round(value, 4), "unit": "committed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                         "sample": f"fp64 oracle, same shape and mode, n={WL.n}, 32-token prompt (prefill untimed), "
+                                   f"{k + w} steps ({dt:.1f} s); tokens/s = steps/s x alpha {alpha:.4f}"},
+        "e2e": {"value": round(e2e_tokens / (e_pf + e_dt), 4), "unit": "generated tokens/s (prefill + decode, host "
+                "buffers)", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "sample": f"prompt {WL.prompt_len} prefilled ({e_pf:.1f} s) + 4 steps ({e_dt:.1f} s); tokens = 1 + "
+                          f"4 x alpha"},
     }
     print(json.dumps(line), flush=True)
 

@@ -28,7 +28,8 @@
  *     internal second stream joined back to it); calls return after issuing work,
  *     except where an argument named *_host receives a result (those synchronise).
  *   - Layout: matrices are row-major [out][in] in the dtype of spd_dims.dtype;
- *     norm gains are fp32 vectors.  KV caches use the weight dtype.
+ *     norm gains are fp32 vectors.  KV caches are fp32 for fp32 weights and fp16 for
+ *     bf16 weights (same bytes as bf16, 8x finer rounding; values saturate at +-65504).
  */
 #ifndef SPD_H
 #define SPD_H
@@ -49,9 +50,11 @@ extern "C" {
 #define SPD_ECAPACITY 5  /* max_seq, max_new or the step-trace capacity would overflow */
 #define SPD_EDEVICE 6    /* a kernel reported an error flag (bounds check failed)      */
 
-/* weight dtypes */
+/* element types: weights are SPD_F32 or SPD_BF16; the KV caches of a handle are fp32 for
+ * fp32 weights and fp16 (SPD_F16) for bf16 weights */
 #define SPD_F32 0
 #define SPD_BF16 1
+#define SPD_F16 2
 
 #define SPD_MAX_ANCHORS 8
 #define SPD_MAX_STAGES 31
@@ -99,7 +102,8 @@ typedef struct spd_pdm_weights {
 
 /* Run configuration.
  *   n            pipeline stages, 1 <= n <= min(L, SPD_MAX_STAGES); stage s holds target
- *                layers [floor(sL/n), floor((s+1)L/n)).
+ *                layers [floor(sL/n), floor((s+1)L/n)) unless stage_bounds says otherwise
+ *                (machine review, "The reading": L/n layers per stage).
  *   anchors      strictly increasing depths in [0, L] with anchors[0] == 0 (the
  *                embedding; the paper reports training is unstable without it,
  *                review "free parameters", App. A.1).  Depth a = residual stream
@@ -116,7 +120,19 @@ typedef struct spd_pdm_weights {
  *                length forced_ref_len; borrowed.
  *   graph        1: each spd_step launch replays a captured CUDA graph of one step.
  *   timing       1: CUDA events bracket every launch of the gate/up projection kernel
- *                (the largest weight stream); read them with spd_kernel_timing. */
+ *                (the largest weight stream); read them with spd_kernel_timing.
+ *   stage_bounds all zero: the uniform split above.  Otherwise the n + 1 layer indices
+ *                0 = b_0 < b_1 < ... < b_n = L, stage s holding layers [b_s, b_{s+1}): a
+ *                non-uniform partition (review, referee report, minor comment on
+ *                Appendix C.1, which gives such assignments without trying them).
+ *   speculate    SPD_SPEC_INPUT: the draft module reads the step's INPUT states and runs
+ *                on a second stream concurrently with the step (the paper's early-start
+ *                schedule).  SPD_SPEC_OUTPUT: it runs after the step's target layers on
+ *                their OUTPUT states (stage s's token at depth b_{s+1}, the exiting token
+ *                at full depth): the input- vs output-state ablation the referee report
+ *                lists.  Tokens and verification are the same; the drafts differ. */
+#define SPD_SPEC_INPUT 0
+#define SPD_SPEC_OUTPUT 1
 typedef struct spd_config {
     int32_t n;
     int32_t n_anchors;
@@ -130,6 +146,8 @@ typedef struct spd_config {
     int32_t forced_ref_len;
     int32_t graph;
     int32_t timing;
+    int32_t stage_bounds[SPD_MAX_STAGES + 1];
+    int32_t speculate;
 } spd_config;
 
 /* Per-run statistics.  N = committed tokens after the prefill's, K = pipeline steps,
@@ -173,26 +191,45 @@ int spd_create(const spd_dims *d, const spd_target_weights *tw, const spd_pdm_we
 /* Prefill (untimed part of the method): run the whole prompt (device int32 ids,
  * 1 <= prompt_len, prompt_len + max_new + n <= max_seq) through all target layers,
  * fill the draft module's cached prefix with full-depth features of every prompt
- * position, pick the first token y0 (committed) and seed stage 0 with it.  Resets
- * the step counter, trace and statistics. */
+ * position (verified prefixes use depth-maximised features: machine review, "What
+ * carries the argument"), pick the first token y0 (committed) and seed stage 0 with
+ * it.  Resets the step counter, trace and statistics.  Errors: SPD_EINVAL (empty
+ * prompt), SPD_ECAPACITY (too long for max_seq), SPD_ECUDA. */
 int spd_prefill(spd_handle *h, const int32_t *prompt_dev, int32_t prompt_len);
 
 /* Issue up to n_steps pipeline steps (steps after completion are no-ops on the
- * device).  If committed_host is non-NULL, synchronise and store 1 + N (tokens
- * generated so far, y0 included).  SPD_ESTATE before spd_prefill. */
+ * device).  One step (machine review, "The reading" and "What carries the argument"):
+ * every occupied stage runs its layers on its own in-flight token; the draft module
+ * proposes the token after the newest one from the anchor states; the token leaving the
+ * last stage yields the target's token, the draft one position behind it is verified
+ * (streaming verification; at T > 0 speculative rejection sampling, review
+ * "Assumptions", section 3.5), and a rejection truncates the KV caches after the exiting
+ * position, flushes the pipeline and reseeds stage 0 with the target's token.  No host
+ * round trip happens inside a step.  If committed_host is non-NULL, synchronise and
+ * store 1 + N (tokens generated so far, y0 included).  Errors: SPD_ESTATE before
+ * spd_prefill, SPD_EINVAL for n_steps < 0, SPD_ECUDA, SPD_EDEVICE (a kernel's error flag,
+ * reported when committed_host is given).  The caller's stream is joined back on every
+ * return after work was issued. */
 int spd_step(spd_handle *h, int32_t n_steps, int32_t *committed_host);
 
-/* Prefill + steps until max_new tokens are committed, polling the device every few
- * steps.  If buffers_on_host is 0, prompt and out_tokens are device pointers;
- * if 1, they are host pointers and the copies happen inside the call.  out_tokens
- * receives max_new ids; *n_out_host (nullable) the count; *stats_host (nullable)
- * the statistics. */
+/* Generation of one sequence (abstract: n tokens of a single sequence advance per
+ * step): spd_prefill, then spd_step batches until max_new tokens are committed,
+ * polling the device between batches (never more steps than tokens still missing).
+ * If buffers_on_host is 0, prompt and out_tokens are device pointers; if 1, they are
+ * host pointers (prompt_len <= max_steps * L) and the copies happen inside the call.
+ * out_tokens receives max_new ids (y0 first); *n_out_host (nullable) the count;
+ * *stats_host (nullable) the statistics.  Errors as spd_prefill and spd_step, plus
+ * SPD_ECAPACITY for a host prompt too long to stage; on every error after work was
+ * issued the caller's stream is still ordered after it. */
 int spd_generate(spd_handle *h, const int32_t *prompt, int32_t prompt_len, int32_t buffers_on_host,
                  int32_t *out_tokens, int32_t *n_out_host, spd_stats *stats_host);
 
 /* Copy the first min(max_recs, K) trace records and, if len_host is non-NULL, the
  * per-layer KV valid lengths after each step ([rec][L] int32) to host memory;
- * *count_host = K.  Synchronises. */
+ * *count_host = K.  The records are what the streaming verification decided each step
+ * (exit position, verified draft, target token, keep flag, committed token; machine
+ * review, "What carries the argument"), and the KV lengths show every truncation.
+ * Synchronises.  SPD_ECUDA on a failed copy. */
 int spd_get_trace(spd_handle *h, spd_trace_rec *recs_host, int32_t max_recs, int32_t *len_host,
                   int32_t *count_host);
 
@@ -206,7 +243,7 @@ int spd_get_tokens(spd_handle *h, int32_t *tokens_host, int32_t max_tokens, int3
 #define SPD_BUF_RESIDUAL 0   /* fp32 [n+1][d]: per-slot residual stream (slot ring)       */
 #define SPD_BUF_ANCHORS 1    /* fp32 [n+1][n_anchors][d]: per-slot anchor states          */
 #define SPD_BUF_LOGITS 2     /* fp32 [2][V]: last step's target-exit and draft logits     */
-#define SPD_BUF_KCACHE 3     /* dtype [max_seq][Hkv][hd] of target layer `index`         */
+#define SPD_BUF_KCACHE 3     /* KV type [max_seq][Hkv][hd] of target layer `index`       */
 #define SPD_BUF_VCACHE 4
 #define SPD_BUF_PDM_KCACHE 5 /* same, draft layer `index`                                */
 #define SPD_BUF_PDM_VCACHE 6
@@ -230,7 +267,8 @@ int spd_kernel_timing(spd_handle *h, double *total_ms_host, int64_t *launches_ho
  * cache): out[h] = softmax(q[h] . K[:, h/G]^T / sqrt(hd)) V[:, h/G] over positions
  * 0..seq_len-1, G = Hq / Hkv.
  *   q      device fp32 [Hq][hd] (already rotated by RoPE)
- *   k, v   device [seq_len][Hkv][hd] in dtype (SPD_F32 or SPD_BF16) — the KV-cache layout
+ *   k, v   device [seq_len][Hkv][hd] in dtype (SPD_F32, SPD_BF16 or SPD_F16) — the KV-cache
+ *          layout
  *   out    device fp32 [Hq][hd]
  *   Hq / Hkv in {1, 2, 4, 8}; hd 64 or 128; 1 <= seq_len <= 16384; q, k, v, out 16-byte
  *   aligned.  Split-K over 128-position chunks merged in chunk order (deterministic).
@@ -247,8 +285,9 @@ int spd_attention_decode(int32_t dtype, int32_t Hq, int32_t Hkv, int32_t hd, int
  * allocator, or a cudaMalloc and its implicit synchronisation is not acceptable where
  * they run.  Same arguments, result and errors as spd_attention_decode minus the
  * scratch: the split-K partials live in a 1 MiB array inside the library, reserved on
- * every GPU that loads it until the process exits (e.g. Hq 32, hd 128: seq_len up to
- * 8064).  Larger shapes fail with SPD_ECAPACITY.  The entry point itself allocates
+ * every GPU that loads it until the process exits.  A call fits when
+ * 256 + Hq * ceil(seq_len / 128) * (hd + 4) * 4 <= 1048576 bytes (e.g. Hq 32, hd 128:
+ * seq_len up to 7936).  Larger shapes fail with SPD_ECAPACITY.  The entry point itself allocates
  * nothing (no cudaMalloc / cudaFree).  Its first call on a device looks up the array's
  * device address for that device (make that first call before any stream capture).
  * Every call shares the array: each clears what must start at zero, and calls that
@@ -259,7 +298,9 @@ int spd_attention_decode_noalloc(int32_t dtype, int32_t Hq, int32_t Hkv, int32_t
 /* Text of the calling thread's last failure of a standalone entry point ("" if none). */
 const char *spd_ops_last_error(void);
 
-/* Return to the post-create state (keeps weights and workspace). */
+/* Return to the post-create state (keeps weights and workspace): the run state
+ * (step counter, committed count, slot ring, statistics) is cleared; the next call must
+ * be spd_prefill or spd_generate.  Synchronises.  SPD_ECUDA on failure. */
 int spd_reset(spd_handle *h);
 
 /* Release streams, events and graphs (not the borrowed memory).  NULL is a no-op. */

@@ -289,6 +289,7 @@ class SPDOracle:
         m = self.m
         feats = np.stack([m.feature(tk.anchors, dep) for (tk, dep) in rows])
         Hp = m.pdm_block(feats, rows[0][0].pos, self.pkv)
+        self.last_Hp = Hp
         zD = m.pdm_logits(Hp[-1])
         if self.replay is not None and self.forced_p is None and self.T == 0.0:
             top = self.replay.pick_argmax(zD, None if rep is None else rep.get("pdm_top"), "pdm", t)

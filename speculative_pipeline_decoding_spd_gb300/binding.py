@@ -13,7 +13,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libspd_gb300.so")
 
 SPD_OK, SPD_EINVAL, SPD_ENOMEM, SPD_ECUDA, SPD_ESTATE, SPD_ECAPACITY, SPD_EDEVICE = range(7)
-SPD_F32, SPD_BF16 = 0, 1
+SPD_F32, SPD_BF16, SPD_F16 = 0, 1, 2
+SPD_SPEC_INPUT, SPD_SPEC_OUTPUT = 0, 1
 SPD_MAX_ANCHORS, SPD_MAX_STAGES, SPD_MAX_LAYERS, SPD_MAX_PDM_LAYERS = 8, 31, 128, 16
 (SPD_BUF_RESIDUAL, SPD_BUF_ANCHORS, SPD_BUF_LOGITS, SPD_BUF_KCACHE, SPD_BUF_VCACHE, SPD_BUF_PDM_KCACHE,
  SPD_BUF_PDM_VCACHE, SPD_BUF_SLOTS, SPD_BUF_STATE, SPD_BUF_PREFILL_LOGITS, SPD_BUF_PDM_RESIDUAL) = range(11)
@@ -48,7 +49,8 @@ class spd_config(C.Structure):
     _fields_ = [("n", C.c_int32), ("n_anchors", C.c_int32), ("anchors", C.c_int32 * SPD_MAX_ANCHORS),
                 ("temperature", C.c_float), ("seed", C.c_uint64), ("max_seq", C.c_int32), ("max_new", C.c_int32),
                 ("force_p", C.c_float), ("forced_ref", C.c_void_p), ("forced_ref_len", C.c_int32),
-                ("graph", C.c_int32), ("timing", C.c_int32)]
+                ("graph", C.c_int32), ("timing", C.c_int32), ("stage_bounds", C.c_int32 * (SPD_MAX_STAGES + 1)),
+                ("speculate", C.c_int32)]
 
 
 class spd_stats(C.Structure):

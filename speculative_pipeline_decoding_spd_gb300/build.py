@@ -37,7 +37,8 @@ def _stale(obj: str, deps) -> bool:
 def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(OUT, exist_ok=True)
     cc = nvcc()
-    header_deps = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "attn.cuh"), os.path.join(HERE, "..", "include", "spd.h")]
+    header_deps = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith(".cuh")]
+    header_deps.append(os.path.join(HERE, "..", "include", "spd.h"))
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)

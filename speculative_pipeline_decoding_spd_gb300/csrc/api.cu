@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -98,7 +99,26 @@ static int validate(const spd_dims *d, int Ls, const spd_config *c, std::string 
         if (c->temperature > 0.f) { why = "forced drafts are defined for T = 0 only"; return SPD_EINVAL; }
     }
     if (c->temperature > 0.f && Ls == 0) { why = "sampling needs a draft module"; return SPD_EINVAL; }
+    if (c->speculate != SPD_SPEC_INPUT && c->speculate != SPD_SPEC_OUTPUT) {
+        why = "speculate must be SPD_SPEC_INPUT or SPD_SPEC_OUTPUT";
+        return SPD_EINVAL;
+    }
+    bool explicit_bounds = false;
+    for (int s = 0; s <= SPD_MAX_STAGES; ++s) explicit_bounds = explicit_bounds || c->stage_bounds[s] != 0;
+    if (explicit_bounds) {
+        bool ok = c->stage_bounds[0] == 0 && c->stage_bounds[c->n] == d->L;
+        for (int s = 0; s < c->n; ++s) ok = ok && c->stage_bounds[s + 1] > c->stage_bounds[s];
+        for (int s = c->n + 1; s <= SPD_MAX_STAGES; ++s) ok = ok && c->stage_bounds[s] == 0;
+        if (!ok) { why = "stage_bounds must be 0 = b_0 < b_1 < ... < b_n = L (zero past b_n)"; return SPD_EINVAL; }
+    }
     return SPD_OK;
+}
+
+// Stage s holds layers [b[s], b[s + 1]): the caller's explicit bounds, else floor(s L / n).
+static void stage_plan(const spd_dims *d, const spd_config *c, int *b) {
+    bool explicit_bounds = false;
+    for (int s = 0; s <= SPD_MAX_STAGES; ++s) explicit_bounds = explicit_bounds || c->stage_bounds[s] != 0;
+    for (int s = 0; s <= c->n; ++s) b[s] = explicit_bounds ? c->stage_bounds[s] : (int)(((long long)s * d->L) / c->n);
 }
 
 static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base, Plan &h) {
@@ -129,7 +149,7 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.Xb = b.take<__nv_bfloat16>((size_t)ns * d->d);
     h.ATTb = b.take<__nv_bfloat16>((size_t)ns * qr);
     h.GUb = b.take<__nv_bfloat16>((size_t)ns * d->F);
-    h.Xlm = b.take<__nv_bfloat16>((size_t)2 * d->d);
+    h.Xlm = b.take<__nv_bfloat16>((size_t)4 * d->d);
     h.ANCHb = b.take<__nv_bfloat16>((size_t)ns * c->n_anchors * d->d);
     h.ssp = b.take<float>((size_t)MAXS * (d->d / 8));
     {
@@ -159,6 +179,10 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.pf_ANCH = b.take<float>((size_t)PF_ROWS * c->n_anchors * d->d);
     h.pf_Hp = b.take<float>((size_t)PF_ROWS * d->d);
     h.pf_logits = b.take<float>((size_t)d->V);
+    {
+        const int kmax = std::max(std::max(d->d, d->F), std::max(qr, c->n_anchors * d->d));
+        h.pf_A2 = b.take<__nv_bfloat16>(d->dtype == SPD_BF16 ? (size_t)2 * PF_ROWS * kmax : 1);
+    }
     Plan *dp = b.take<Plan>(1);
     h.self = dp;
     h.kv_stride = kvs;
@@ -183,8 +207,9 @@ template <typename T>
 static void record_step(spd_handle *H, std::vector<int> *pairs) {
     const Plan &h = H->h;
     Plan *P = H->dP;
-    // draft module on the second stream, concurrent with the target's rounds
-    const bool separate = h.Ls > 0;
+    // input-state schedule: the draft module on the second stream, concurrent with the
+    // target's rounds; output-state schedule: on the target's stream after its rounds
+    const bool separate = h.Ls > 0 && !h.spec_out;
     if (separate) {
         cudaEventRecord(H->ev_fork, H->s_main);
         cudaStreamWaitEvent(H->s_pdm, H->ev_fork, 0);
@@ -209,6 +234,7 @@ static void record_step(spd_handle *H, std::vector<int> *pairs) {
         launch_target_down<T>(P, h, j, H->grid_gemv, H->s_main);
     }
     if (separate) cudaStreamWaitEvent(H->s_main, H->ev_join, 0);
+    if (h.Ls > 0 && h.spec_out) launch_pdm_step<T>(P, h, H->num_sms, H->s_main);
     launch_lm_head<T>(P, h, H->grid_lm, H->s_main);
     launch_verify<T>(P, h, H->s_main);
 }
@@ -293,8 +319,9 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
     h.n = c->n; h.nB = c->n_anchors; h.Ls = Ls; h.max_seq = c->max_seq; h.max_new = c->max_new; h.dtype = d->dtype;
     h.q_rows = d->Hq * d->hd; h.kv_rows = d->Hkv * d->hd; h.qkv_rows = h.q_rows + 2 * h.kv_rows;
     h.J = 0;
-    for (int s = 0; s <= c->n; ++s) h.b[s] = (int)(((long long)s * d->L) / c->n);
+    stage_plan(d, c, h.b);
     for (int s = 0; s < c->n; ++s) h.J = std::max(h.J, h.b[s + 1] - h.b[s]);
+    h.spec_out = c->speculate == SPD_SPEC_OUTPUT ? 1 : 0;
     for (int a = 0; a <= SPD_MAX_LAYERS; ++a) h.aidx[a] = -1;
     for (int i = 0; i < c->n_anchors; ++i) {
         h.anchors[i] = c->anchors[i];
@@ -350,6 +377,17 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
     }
     pdm_plan(h.d, h.F, h.q_rows, h.nB, h.n, h.dtype, h.pdm_kx, h.pdm_ns, &h.pdm_MT);
     h.pdl = 1;
+    // Test hooks for the bounded waits, read once here and off unless set:
+    // SPD_TEST_WAIT_CYCLES=<n> bounds the grouped GEMV's mbarrier waits at n SM cycles instead
+    // of about 2 s; SPD_TEST_WITHHOLD_TILE=1 makes the first step's first gate/up launch skip
+    // loading one tile, so a wait runs out and the step reports SPD_EDEVICE (ERR_TIMEOUT).
+    h.wait_cycles = WAIT_LIMIT_CYCLES;
+    h.test_withhold = 0;
+    if (const char *e = std::getenv("SPD_TEST_WAIT_CYCLES")) {
+        const long long v = std::atoll(e);
+        if (v > 0) h.wait_cycles = v;
+    }
+    if (const char *e = std::getenv("SPD_TEST_WITHHOLD_TILE")) h.test_withhold = std::atoi(e) == 1 ? 1 : 0;
     const int gsm = gemv_smem_bytes(h);
     set_target_attributes(std::max(gsm, 48 * 1024));
     set_pdm_attributes();
@@ -380,7 +418,7 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
         cudaMemsetAsync(h.patt_cnt, 0, sizeof(int) * MAXS * h.Hkv, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.pdm_cnt, 0, sizeof(int) * SM_BOUND, H->s_main) != cudaSuccess ||
         cudaMemsetAsync(h.lm_cnt, 0, sizeof(int), H->s_main) != cudaSuccess ||
-        cudaMemsetAsync(h.Xlm, 0, sizeof(__nv_bfloat16) * 2 * h.d, H->s_main) != cudaSuccess) {
+        cudaMemsetAsync(h.Xlm, 0, sizeof(__nv_bfloat16) * 4 * h.d, H->s_main) != cudaSuccess) {
         H->err = "workspace initialisation failed";
         return bail(SPD_ECUDA);
     }
@@ -418,10 +456,13 @@ extern "C" int spd_prefill(spd_handle *H, const int32_t *prompt, int32_t prompt_
         return fail(H, SPD_ECAPACITY, "prompt_len + max_new + n exceeds max_seq");
     int rc = enter(H);
     if (rc) return rc;
-    if (H->h.dtype == SPD_BF16) launch_prefill<__nv_bfloat16>(H->dP, H->h, prompt, prompt_len, H->grid_gemv, H->s_main);
-    else launch_prefill<float>(H->dP, H->h, prompt, prompt_len, H->grid_gemv, H->s_main);
-    CK(H, cudaGetLastError());
+    const int enc = H->h.dtype == SPD_BF16
+                        ? launch_prefill<__nv_bfloat16>(H->dP, H->h, prompt, prompt_len, H->num_sms, H->s_main)
+                        : launch_prefill<float>(H->dP, H->h, prompt, prompt_len, H->num_sms, H->s_main);
+    const cudaError_t le = cudaGetLastError();
     rc = leave(H);
+    if (enc) return fail(H, SPD_ECUDA, "prefill: a TMA tensor map could not be encoded");
+    if (le != cudaSuccess) return fail(H, SPD_ECUDA, std::string("prefill launch: ") + cudaGetErrorString(le));
     if (rc) return rc;
     H->prefilled = true;
     H->t_ms = 0.0;
@@ -491,7 +532,12 @@ extern "C" int spd_step(spd_handle *H, int32_t n_steps, int32_t *committed_host)
     int rc = enter(H);
     if (rc) return rc;
     rc = run_steps(H, n_steps);
-    if (rc) return rc;
+    if (rc) {
+        const std::string keep = H->err;
+        leave(H);
+        H->err = keep;
+        return rc;
+    }
     rc = leave(H);
     if (rc) return rc;
     if (committed_host) {
@@ -527,38 +573,51 @@ extern "C" int spd_generate(spd_handle *H, const int32_t *prompt, int32_t prompt
                             int32_t *n_out_host, spd_stats *stats_host) {
     if (!H) return SPD_EINVAL;
     if (!prompt || !out_tokens) return fail(H, SPD_EINVAL, "null prompt/out");
+    if (on_host && (prompt_len < 1 || (size_t)prompt_len > (size_t)H->h.max_steps * H->h.L))
+        return fail(H, SPD_ECAPACITY, "prompt too long for host staging");
     const int32_t *pdev = prompt;
-    int rc0 = enter(H);
-    if (rc0) return rc0;
+    int rc = enter(H);
+    if (rc) return rc;
+    // every exit after enter() orders the caller's stream after the work issued so far
+    auto finish = [&](int code) {
+        const std::string keep = H->err;
+        const int lrc = leave(H);
+        if (code) {
+            H->err = keep;
+            return code;
+        }
+        return lrc;
+    };
     if (on_host) {
         // the prompt is staged in the per-step KV-length trace, unused until the first step
-        if (prompt_len < 1 || (size_t)prompt_len > (size_t)H->h.max_steps * H->h.L)
-            return fail(H, SPD_ECAPACITY, "prompt too long for host staging");
-        CK(H, cudaMemcpyAsync(H->h.trace_len, prompt, (size_t)prompt_len * sizeof(int), cudaMemcpyHostToDevice, H->s_main));
+        const cudaError_t e = cudaMemcpyAsync(H->h.trace_len, prompt, (size_t)prompt_len * sizeof(int),
+                                              cudaMemcpyHostToDevice, H->s_main);
+        if (e != cudaSuccess) return finish(fail(H, SPD_ECUDA, std::string("prompt copy: ") + cudaGetErrorString(e)));
         pdev = H->h.trace_len;
     }
-    int rc = spd_prefill(H, pdev, prompt_len);
-    if (rc) return rc;
+    rc = spd_prefill(H, pdev, prompt_len);
+    if (rc) return finish(rc);
     const int max_new = H->h.max_new;
     int N = 0, done = 0, err = 0;
     rc = read_state(H, &N, &done, &err);
-    if (rc) return rc;
+    if (rc) return finish(rc);
     long long issued = 0;
     while (!done && 1 + N < max_new) {
-        if (issued >= H->h.max_steps) return fail(H, SPD_EDEVICE, "no progress within the step bound");
+        if (issued >= H->h.max_steps) return finish(fail(H, SPD_EDEVICE, "no progress within the step bound"));
         int left = max_new - (1 + N);
         int k = left >= GRAPH_STEPS ? GRAPH_STEPS : left;
         rc = run_steps(H, k);
-        if (rc) return rc;
+        if (rc) return finish(rc);
         issued += k;
         rc = read_state(H, &N, &done, &err);
-        if (rc) return rc;
-        if (err) return fail(H, SPD_EDEVICE, "device error flag " + std::to_string(err));
+        if (rc) return finish(rc);
+        if (err) return finish(fail(H, SPD_EDEVICE, "device error flag " + std::to_string(err)));
     }
-    CK(H, cudaMemcpyAsync(out_tokens, H->h.out_tokens, (size_t)max_new * sizeof(int),
-                          on_host ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice, H->s_main));
-    CK(H, cudaStreamSynchronize(H->s_main));
-    rc = leave(H);
+    cudaError_t e = cudaMemcpyAsync(out_tokens, H->h.out_tokens, (size_t)max_new * sizeof(int),
+                                    on_host ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice, H->s_main);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(H->s_main);
+    if (e != cudaSuccess) return finish(fail(H, SPD_ECUDA, std::string("token copy: ") + cudaGetErrorString(e)));
+    rc = finish(SPD_OK);
     if (rc) return rc;
     if (n_out_host) *n_out_host = 1 + N;
     if (stats_host) return spd_get_stats(H, stats_host);

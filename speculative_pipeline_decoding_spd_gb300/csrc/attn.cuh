@@ -31,13 +31,26 @@ constexpr int ATT_HB = 4;       // heads per weighted-sum pass
 // 2K-position context
 template <typename T> __host__ __device__ constexpr int att_min_blocks() { return sizeof(T) == 2 ? 3 : 1; }
 
-// K and V rows live in shared memory as 32-bit words: bf16 pairs (T = bf16) or floats.
-template <typename T> struct KVW {
+// K and V rows live in shared memory as 32-bit words: 16-bit pairs (T = fp16 or bf16) or
+// floats.  lo / hi widen the first / second element of a pair.
+template <typename T> struct KVW;
+template <> struct KVW<__nv_bfloat16> {
     static constexpr int PER = 2;   // elements per word
     __device__ static __forceinline__ uint32_t pack(float a, float b) {
         const __nv_bfloat16 x = __float2bfloat16_rn(a), y = __float2bfloat16_rn(b);
         return (uint32_t)__bfloat16_as_ushort(x) | ((uint32_t)__bfloat16_as_ushort(y) << 16);
     }
+    __device__ static __forceinline__ float lo(uint32_t u) { return bf_lo(u); }
+    __device__ static __forceinline__ float hi(uint32_t u) { return bf_hi(u); }
+};
+template <> struct KVW<__half> {
+    static constexpr int PER = 2;
+    __device__ static __forceinline__ uint32_t pack(float a, float b) {
+        const __half x = __float2half_rn(a), y = __float2half_rn(b);
+        return (uint32_t)__half_as_ushort(x) | ((uint32_t)__half_as_ushort(y) << 16);
+    }
+    __device__ static __forceinline__ float lo(uint32_t u) { return h_lo(u); }
+    __device__ static __forceinline__ float hi(uint32_t u) { return h_hi(u); }
 };
 template <> struct KVW<float> {
     static constexpr int PER = 1;
@@ -147,13 +160,13 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
             const auto k1 = WTraits<T>::store(x1 * r.x + x0 * r.y);
             kdst[i] = k0;
             kdst[i + half] = k1;
-            knew[i] = (float)k0;
-            knew[i + half] = (float)k1;
+            knew[i] = WTraits<T>::get(&k0, 0);
+            knew[i + half] = WTraits<T>::get(&k1, 0);
         } else if (tid < half + hd) {
             const int i = tid - half;
             const auto v0 = WTraits<T>::store(vh[i]);
             vdst[i] = v0;
-            vnew[i] = (float)v0;
+            vnew[i] = WTraits<T>::get(&v0, 0);
         }
     }
     cp_async_wait_all();
@@ -186,8 +199,8 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
                 float k[8];
                 int e0;   // element index of kw.x
                 if constexpr (KVW<T>::PER == 2) {
-                    k[0] = bf_lo(kw.x); k[1] = bf_hi(kw.x); k[2] = bf_lo(kw.y); k[3] = bf_hi(kw.y);
-                    k[4] = bf_lo(kw.z); k[5] = bf_hi(kw.z); k[6] = bf_lo(kw.w); k[7] = bf_hi(kw.w);
+                    k[0] = KVW<T>::lo(kw.x); k[1] = KVW<T>::hi(kw.x); k[2] = KVW<T>::lo(kw.y); k[3] = KVW<T>::hi(kw.y);
+                    k[4] = KVW<T>::lo(kw.z); k[5] = KVW<T>::hi(kw.z); k[6] = KVW<T>::lo(kw.w); k[7] = KVW<T>::hi(kw.w);
                     e0 = 2 * w;
                 } else {
                     k[0] = __uint_as_float(kw.x); k[1] = __uint_as_float(kw.y);
@@ -255,8 +268,8 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
             const uint4 vw = *reinterpret_cast<const uint4 *>(Vs + j * KP + 4 * vo);
             float v[EPV];
             if constexpr (sizeof(T) == 2) {
-                v[0] = bf_lo(vw.x); v[1] = bf_hi(vw.x); v[2] = bf_lo(vw.y); v[3] = bf_hi(vw.y);
-                v[4] = bf_lo(vw.z); v[5] = bf_hi(vw.z); v[6] = bf_lo(vw.w); v[7] = bf_hi(vw.w);
+                v[0] = KVW<T>::lo(vw.x); v[1] = KVW<T>::hi(vw.x); v[2] = KVW<T>::lo(vw.y); v[3] = KVW<T>::hi(vw.y);
+                v[4] = KVW<T>::lo(vw.z); v[5] = KVW<T>::hi(vw.z); v[6] = KVW<T>::lo(vw.w); v[7] = KVW<T>::hi(vw.w);
             } else {
                 v[0] = __uint_as_float(vw.x); v[1] = __uint_as_float(vw.y);
                 v[2] = __uint_as_float(vw.z); v[3] = __uint_as_float(vw.w);

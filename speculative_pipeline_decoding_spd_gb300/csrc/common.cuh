@@ -9,12 +9,14 @@
 //   QKV fp32 [n][(Hq+2Hkv) hd]   raw q,k,v of each stage (RoPE is applied by the attention kernel)
 //   att_part fp32 [stage][Hq][chunk][hd+4]  attention chunk partials (merged by the O projection)
 //   U   fp32 [n][2F]             raw gate and up sums of each stage (SiLU(gate)*up formed by the down GEMV)
-//   K/V cache per target layer   dtype [max_seq][Hkv][hd]; valid length per layer in DevState
+//   K/V cache per target layer   [max_seq][Hkv][hd] in the KV type (fp16 for bf16 weights, fp32 for
+//                                fp32 weights); valid length per layer in DevState
 //   draft module buffers         Xp [n+1][d], QKVp/ATTp/GUp per row, its own K/V cache
 //   logits fp32 [2][V]           row 0 = target prediction of the exiting token, row 1 = draft
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,6 +67,7 @@ struct Plan {
     int qkv_rows, q_rows, kv_rows;
     int J;                         // rounds per step = longest stage
     int b[MAXS + 1];               // stage bounds
+    int spec_out;                  // 1: the draft module runs after the step on its output states
     int anchors[MAXB];
     signed char aidx[MAXL + 1];    // anchor index of depth a, or -1
     float eps, scale, temperature;
@@ -96,12 +99,15 @@ struct Plan {
     __nv_bfloat16 *ATTb;           // [n+1][Hq hd] attention output
     __nv_bfloat16 *GUb;            // [n+1][F] SiLU(gate) * up
     __nv_bfloat16 *ANCHb;          // [n+1][nB][d] the anchor states as bf16 (the draft projection's input)
-    __nv_bfloat16 *Xlm;            // [2][d] LM head rows: x * g_final of the exiting token and of the draft's newest row
+    __nv_bfloat16 *Xlm;            // [4][d] LM head rows: x * g_final of the exiting token and of the draft's newest row
+                                   // (rows 0, 1: bf16 of the value; rows 2, 3: bf16 of what rows 0, 1 left out)
     float *pdm_part;               // draft GEMM K-slab partials [slab][n+1][N]
     int *pdm_cnt;                  // draft GEMM row-block arrival counters (zero between launches)
     int pdm_kx[6], pdm_ns[6];      // draft-style GEMMs (proj, qkv, o, gate/up, down, LM head): K slab width, slabs
     int pdm_MT;                    // 16-row mma tiles of the draft rows (1: n+1 <= 16, else 2)
     int pdl;                       // step kernels launched with programmatic dependent launch
+    long long wait_cycles;         // bound of the grouped GEMV's mbarrier waits (SM cycles)
+    int test_withhold;             // test hook: 1 = the first gate/up launch's CTA 0 never loads its last tile
     float *logits;                 // [2][V]
     float *dlogits;                // [n+1][V] draft logits per slot (T > 0)
     float *lm_part;                // [grid][2] (val, idx as float bits)
@@ -114,6 +120,8 @@ struct Plan {
     int pf_rows;                   // rows per prefill chunk
     float *pf_H, *pf_XN, *pf_QKV, *pf_ATT, *pf_GU, *pf_ANCH, *pf_Hp;
     float *pf_logits;              // [V]
+    __nv_bfloat16 *pf_A2;          // bf16 weights: the tensor-core GEMMs' input rows as two bf16 parts,
+                                   // hi [pf_rows][K] then lo [pf_rows][K], K the consuming GEMM's width
     Plan *self;                    // device address of this plan
 };
 
@@ -141,13 +149,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;   // ~2 s of SM clock: far beyond any legitimate wait
-// Wait for the completion of the phase with this parity; false after WAIT_LIMIT_CYCLES.
+// Wait for the completion of the phase with this parity; false after `limit` cycles.
 // The bound uses the SM's own cycle counter, which is cheap to read inside the spin.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit = WAIT_LIMIT_CYCLES) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
+        if (clock64() - t0 > limit) return false;
     return true;
 }
 // 1-D bulk copy global -> this CTA's shared memory; completion counted in bytes on bar.
@@ -194,6 +202,22 @@ template <> struct WTraits<__nv_bfloat16> {
     __device__ static __forceinline__ float get(const __nv_bfloat16 *p, long long i) { return __bfloat162float(p[i]); }
     __device__ static __forceinline__ __nv_bfloat16 store(float v) { return __float2bfloat16_rn(v); }
 };
+// fp16: the KV cache of bf16 models (same bytes as bf16, three more mantissa bits).  Values
+// beyond the fp16 range saturate at +-65504 instead of becoming infinite.
+constexpr float F16_MAX = 65504.f;
+template <> struct WTraits<__half> {
+    static constexpr int VEC = 8;
+    __device__ static __forceinline__ float get(const __half *p, long long i) { return __half2float(p[i]); }
+    __device__ static __forceinline__ __half store(float v) { return __float2half_rn(fminf(fmaxf(v, -F16_MAX), F16_MAX)); }
+};
+
+// Element type of the K/V caches for weights of type T: fp32 for fp32 models, fp16 for bf16
+// models.  K and V are O(1) activations, so fp16's range holds them; its finer mantissa keeps
+// the cache's rounding (the largest difference from exact arithmetic in a bf16 model) 8x
+// smaller than a bf16 cache would.
+template <typename T> struct KvOf { using type = T; };
+template <> struct KvOf<__nv_bfloat16> { using type = __half; };
+template <typename T> using KvT = typename KvOf<T>::type;
 
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     uint4 r;
@@ -205,6 +229,8 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float h_lo(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u & 0xffffu))); }
+__device__ __forceinline__ float h_hi(uint32_t u) { return __half2float(__ushort_as_half((unsigned short)(u >> 16))); }
 
 // Dot product of one 16-byte weight vector with the matching x values (fixed order).
 __device__ __forceinline__ float dot16(const uint4 &w, const float *x, float acc, __nv_bfloat16) {
@@ -408,17 +434,26 @@ __device__ __forceinline__ void warp_stage_list(const Plan *__restrict__ P, int 
     __syncwarp();
 }
 
+// The draft module has a full-depth row for the token that left the pipeline in the
+// previous step only under the input-state schedule; under the output-state schedule that
+// token was at full depth in its own step already.
+__device__ __forceinline__ int pdm_pending(const Plan *__restrict__ P, const DevState *st) {
+    return P->spec_out ? 0 : st->pending;
+}
+
+// Input-state schedule: stage s's row at its input depth b_s; output-state schedule (the
+// module runs after the step's target layers): at its output depth b_{s+1}.
 __device__ __forceinline__ void warp_pdm_rows(const Plan *__restrict__ P, PdmRows &pr, int *done) {
     const int lane = threadIdx.x & 31;
     const DevState *st = P->st;
-    const int n = P->n, head = st->head, pending = st->pending;
+    const int n = P->n, head = st->head, pending = pdm_pending(P, st);
     bool v = false;
     int slot = 0, pos = 0, depth = 0;
     if (lane < n) {
         slot = ring(head, lane, n + 1);
         v = st->valid[slot] != 0;
         pos = st->pos[slot];
-        depth = P->b[lane];
+        depth = P->b[lane + P->spec_out];
     } else if (lane == n && pending) {
         slot = ring(head, n, n + 1);
         pos = st->pos[slot];
@@ -482,7 +517,8 @@ void set_prefill_attributes();
 void set_attn_attributes();
 int attn_smem_bytes(int dtype, int hd, int G);
 template <typename T> void launch_verify(const Plan *P, const Plan &h, cudaStream_t s);
-template <typename T> void launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int grid,
+// returns nonzero when a tensor map could not be encoded (nothing further was launched)
+template <typename T> int launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int num_sms,
                                           cudaStream_t s);
 template <typename T> void launch_prefill_finalize(const Plan *P, int prompt_len, cudaStream_t s);
 void launch_rope_table(const Plan &h, float theta, cudaStream_t s);

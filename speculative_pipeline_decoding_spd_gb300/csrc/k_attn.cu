@@ -18,7 +18,8 @@ namespace spd {
 // (TARGET, round `arg`) or the draft module's rows at draft layer `arg` (their K,V were
 // appended by the draft QKV epilogue).
 template <typename T, bool TARGET>
-__global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const Plan *__restrict__ P, int arg) {
+__global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<KvT<T>>()) k_attn(const Plan *__restrict__ P, int arg) {
+    using KV = KvT<T>;
     __shared__ int s_ok, s_pos, s_layer, s_src;
     const int Hkv = P->Hkv, hd = P->hd;
     const int g = blockIdx.x % Hkv, c = blockIdx.x / Hkv, prob = blockIdx.y;
@@ -53,10 +54,10 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const
     __syncthreads();
     if (!s_ok) return;
     if (!TARGET) pdl_wait();   // the rows' K,V were appended by the preceding draft QKV launch
-    AttnArgs<T> a{};
+    AttnArgs<KV> a{};
     const long long kvoff = (long long)s_layer * P->kv_stride;
-    a.kc = reinterpret_cast<T *>(TARGET ? P->kc : P->pkc) + kvoff;
-    a.vc = reinterpret_cast<T *>(TARGET ? P->vc : P->pvc) + kvoff;
+    a.kc = reinterpret_cast<KV *>(TARGET ? P->kc : P->pkc) + kvoff;
+    a.vc = reinterpret_cast<KV *>(TARGET ? P->vc : P->pvc) + kvoff;
     a.S = s_pos + 1;
     a.maxch = P->att_max_chunks;
     a.Hq = P->Hq;
@@ -85,11 +86,11 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn(const
         a.cnt = P->patt_cnt;
         a.prob = s_src;
     }
-    attn_cta<T>(a, g, c);
+    attn_cta<KV>(a, g, c);
 }
 
 int attn_smem_bytes(int dtype, int hd, int G) {
-    return dtype == SPD_BF16 ? att_smem_bytes<__nv_bfloat16>(hd, G) : att_smem_bytes<float>(hd, G);
+    return dtype == SPD_BF16 ? att_smem_bytes<KvT<__nv_bfloat16>>(hd, G) : att_smem_bytes<float>(hd, G);
 }
 
 void set_attn_attributes() {
@@ -98,9 +99,9 @@ void set_attn_attributes() {
     cudaFuncSetAttribute(k_attn<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          att_smem_bytes<float>(ATT_MAXHD, ATT_MAXG));
     cudaFuncSetAttribute(k_attn<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         att_smem_bytes<__nv_bfloat16>(ATT_MAXHD, ATT_MAXG));
+                         att_smem_bytes<KvT<__nv_bfloat16>>(ATT_MAXHD, ATT_MAXG));
     cudaFuncSetAttribute(k_attn<__nv_bfloat16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         att_smem_bytes<__nv_bfloat16>(ATT_MAXHD, ATT_MAXG));
+                         att_smem_bytes<KvT<__nv_bfloat16>>(ATT_MAXHD, ATT_MAXG));
     cudaFuncSetAttribute(k_attn<float, true>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     cudaFuncSetAttribute(k_attn<float, false>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     cudaFuncSetAttribute(k_attn<__nv_bfloat16, true>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -112,12 +113,12 @@ void set_attn_attributes() {
 template <typename T>
 void launch_target_attn(const Plan *P, const Plan &h, int round, cudaStream_t s) {
     dim3 grid(h.att_max_chunks * h.Hkv, h.n);
-    launch_k(k_attn<T, true>, grid, dim3(ATT_THREADS), att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s, h.pdl != 0, P, round);
+    launch_k(k_attn<T, true>, grid, dim3(ATT_THREADS), att_smem_bytes<KvT<T>>(h.hd, h.Hq / h.Hkv), s, h.pdl != 0, P, round);
 }
 template <typename T>
 void launch_pdm_attn(const Plan *P, const Plan &h, int layer, cudaStream_t s) {
     dim3 grid(h.att_max_chunks * h.Hkv, h.n + 1);
-    launch_k(k_attn<T, false>, grid, dim3(ATT_THREADS), att_smem_bytes<T>(h.hd, h.Hq / h.Hkv), s, h.pdl != 0, P, layer);
+    launch_k(k_attn<T, false>, grid, dim3(ATT_THREADS), att_smem_bytes<KvT<T>>(h.hd, h.Hq / h.Hkv), s, h.pdl != 0, P, layer);
 }
 
 template void launch_target_attn<float>(const Plan *, const Plan &, int, cudaStream_t);

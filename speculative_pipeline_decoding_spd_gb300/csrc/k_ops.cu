@@ -29,7 +29,8 @@ size_t attn_scratch_bytes(int Hq, int Hkv, int hd, int seq_len) {
 
 int attn_validate(int dtype, int Hq, int Hkv, int hd, int seq_len, const void *q, const void *k, const void *v,
                   const void *out) {
-    if (dtype != SPD_F32 && dtype != SPD_BF16) return ops_fail(SPD_EINVAL, "dtype must be SPD_F32 or SPD_BF16");
+    if (dtype != SPD_F32 && dtype != SPD_BF16 && dtype != SPD_F16)
+        return ops_fail(SPD_EINVAL, "dtype must be SPD_F32, SPD_BF16 or SPD_F16");
     if (Hq < 1 || Hkv < 1 || Hq % Hkv) return ops_fail(SPD_EINVAL, "need Hq % Hkv == 0");
     const int G = Hq / Hkv;
     if (G > 8 || (G & (G - 1))) return ops_fail(SPD_EINVAL, "Hq / Hkv must be 1, 2, 4 or 8");
@@ -47,6 +48,17 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<T>()) k_attn_direc
     attn_cta<T>(a, blockIdx.x % a.Hkv, blockIdx.x / a.Hkv);
 }
 
+template <typename T>
+void attn_launch_t(int Hq, int Hkv, int hd, int seq_len, const float *q, const void *k, const void *v, float *out,
+                   float *part, int *cnt, int nch, cudaStream_t s) {
+    AttnArgs<T> a{q, nullptr, nullptr, nullptr, const_cast<T *>(reinterpret_cast<const T *>(k)),
+                  const_cast<T *>(reinterpret_cast<const T *>(v)), seq_len, out, part, cnt, 0, nch, Hq, Hkv, hd,
+                  1.0f / sqrtf((float)hd)};
+    const int sm = att_smem_bytes<T>(hd, Hq / Hkv);
+    cudaFuncSetAttribute(k_attn_direct<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    k_attn_direct<T><<<dim3(nch * Hkv), ATT_THREADS, sm, s>>>(a);
+}
+
 // Launch over (chunks x Hkv) CTAs with scratch = [counters | partials]; counters are
 // cleared on the stream first.
 int attn_launch(int dtype, int Hq, int Hkv, int hd, int seq_len, const float *q, const void *k, const void *v,
@@ -56,23 +68,9 @@ int attn_launch(int dtype, int Hq, int Hkv, int hd, int seq_len, const float *q,
     float *part = reinterpret_cast<float *>(scratch + align256((size_t)Hkv * sizeof(int)));
     cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)Hkv * sizeof(int), s);
     if (e != cudaSuccess) return ops_fail(SPD_ECUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
-    const dim3 grid(nch * Hkv);
-    if (dtype == SPD_BF16) {
-        AttnArgs<__nv_bfloat16> a{q, nullptr, nullptr, nullptr,
-                                  const_cast<__nv_bfloat16 *>(reinterpret_cast<const __nv_bfloat16 *>(k)),
-                                  const_cast<__nv_bfloat16 *>(reinterpret_cast<const __nv_bfloat16 *>(v)), seq_len,
-                                  out, part, cnt, 0, nch, Hq, Hkv, hd, 1.0f / sqrtf((float)hd)};
-        const int sm = att_smem_bytes<__nv_bfloat16>(hd, Hq / Hkv);
-        cudaFuncSetAttribute(k_attn_direct<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        k_attn_direct<__nv_bfloat16><<<grid, ATT_THREADS, sm, s>>>(a);
-    } else {
-        AttnArgs<float> a{q, nullptr, nullptr, nullptr, const_cast<float *>(reinterpret_cast<const float *>(k)),
-                          const_cast<float *>(reinterpret_cast<const float *>(v)), seq_len, out, part, cnt, 0, nch, Hq,
-                          Hkv, hd, 1.0f / sqrtf((float)hd)};
-        const int sm = att_smem_bytes<float>(hd, Hq / Hkv);
-        cudaFuncSetAttribute(k_attn_direct<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        k_attn_direct<float><<<grid, ATT_THREADS, sm, s>>>(a);
-    }
+    if (dtype == SPD_BF16) attn_launch_t<__nv_bfloat16>(Hq, Hkv, hd, seq_len, q, k, v, out, part, cnt, nch, s);
+    else if (dtype == SPD_F16) attn_launch_t<__half>(Hq, Hkv, hd, seq_len, q, k, v, out, part, cnt, nch, s);
+    else attn_launch_t<float>(Hq, Hkv, hd, seq_len, q, k, v, out, part, cnt, nch, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return ops_fail(SPD_ECUDA, std::string("attention launch: ") + cudaGetErrorString(e));
     return SPD_OK;

@@ -4,7 +4,8 @@
 // launch per GEMM (one CTA per SM, the CTA code in pdm.cuh) and one per attention
 // (k_attn.cu).  Its rows' inputs are the step's input states, so nothing in it waits for
 // the target's rounds of the same step; the LM head waits for both streams.  With bf16
-// weights and a tied head the LM head is the same GEMM over two rows (OP_LM).
+// weights and a tied head the LM head is the same GEMM over two rows (OP_LM), each given as
+// two bf16 parts (the value and the rest) whose products are added.
 #include "pdm.cuh"
 
 namespace spd {
@@ -49,7 +50,7 @@ void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[6], int
     *MT = rows <= 16 ? 1 : 2;
     const int Ks[6] = {nB * d, d, q_rows, d, F, d};
     for (int i = 0; i < 6; ++i) {
-        kx[i] = pg_slab(Ks[i], i == OP_LM ? 2 : rows, esz);
+        kx[i] = pg_slab(Ks[i], i == OP_LM ? 4 : rows, esz);   // LM head: two rows, each as two bf16 parts
         ns[i] = (Ks[i] + kx[i] - 1) / kx[i];
     }
 }

@@ -5,9 +5,16 @@
 // the argument": verified positions use every anchor depth).
 //
 // The prompt is processed in chunks of pf_rows positions (each chunk attends causally to
-// the cache of the chunks before it), with an fp32 tiled CUDA-core GEMM (weights bf16 or
-// fp32) and a tiled causal attention whose K/V tiles are staged in shared memory.
-#include "common.cuh"
+// the cache of the chunks before it).  bf16 weights: every projection is a tensor-core
+// GEMM (umma.cuh: tcgen05, TMEM accumulators, TMA-fed operands) whose activation operand
+// comes as two bf16 parts written by the kernel before it (the norm, the attention
+// output's split, SiLU(gate) * up, the anchors' split).  fp32 weights: an fp32 tiled
+// CUDA-core GEMM.  The causal attention stages K/V tiles in shared memory.
+#include <cudaTypedefs.h>
+
+#include <string>
+
+#include "umma.cuh"
 
 namespace spd {
 
@@ -225,6 +232,47 @@ __global__ void __launch_bounds__(256) k_pf_attn(const Plan *__restrict__ P, con
     }
 }
 
+// ---- the tensor-core GEMMs' activation operand: two bf16 parts per value ------------------
+__device__ __forceinline__ void split_store(__nv_bfloat16 *A2, long long lo_off, long long i, float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    A2[i] = hi;
+    A2[lo_off + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// rms(x) * g of every row, written as the hi / lo parts of A2 (row pitch d)
+__global__ void k_pf_norm_split(const float *__restrict__ src, __nv_bfloat16 *__restrict__ A2, int rows_cap,
+                                const float *__restrict__ g, int d, float eps) {
+    __shared__ float red[40];
+    const float *x = src + (long long)blockIdx.x * d;
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < d; k += blockDim.x) ss = fmaf(x[k], x[k], ss);
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    const long long lo = (long long)rows_cap * d;
+    for (int k = threadIdx.x; k < d; k += blockDim.x)
+        split_store(A2, lo, (long long)blockIdx.x * d + k, (x[k] * inv) * g[k]);
+}
+
+// rows of src (pitch ld, K values each) as the hi / lo parts of A2 (row pitch K)
+__global__ void k_pf_split(const float *__restrict__ src, int ld, int K, int M, __nv_bfloat16 *__restrict__ A2,
+                           int rows_cap) {
+    const long long total = (long long)M * K, lo = (long long)rows_cap * K;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+        const long long m = i / K, k = i - m * K;
+        split_store(A2, lo, i, src[m * ld + k]);
+    }
+}
+
+// SiLU(gate) * up of every row as the hi / lo parts of A2 (row pitch F)
+__global__ void k_pf_silu_split(const Plan *__restrict__ P, int M) {
+    const int F = P->F;
+    const long long total = (long long)M * F, lo = (long long)P->pf_rows * F;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+        const long long m = i / F, k = i - m * F;
+        split_store(P->pf_A2, lo, i, silu_f(P->pf_GU[m * 2 * F + k]) * P->pf_GU[m * 2 * F + F + k]);
+    }
+}
+
 __global__ void k_pf_silu(const Plan *__restrict__ P, int M) {
     const int F = P->F;
     const long long total = (long long)M * F;
@@ -266,53 +314,130 @@ __global__ void __launch_bounds__(256) k_pf_logits(const Plan *__restrict__ P, c
 }
 
 // ---------------------------------------------------------------------------------
-template <typename T>
-static void pf_layer(const Plan *P, const Plan &h, const LayerW &w, T *kc, T *vc, float *H, int p0, int M,
-                     cudaStream_t s) {
-    const int d = h.d;
-    k_pf_norm<<<M, 256, 0, s>>>(H, h.pf_XN, w.g1, d, h.eps);
-    pf_gemm<T>(h.pf_XN, d, w.wq, h.q_rows, d, h.pf_QKV, h.qkv_rows, M, 0, s);
-    pf_gemm<T>(h.pf_XN, d, w.wk, h.kv_rows, d, h.pf_QKV + h.q_rows, h.qkv_rows, M, 0, s);
-    pf_gemm<T>(h.pf_XN, d, w.wv, h.kv_rows, d, h.pf_QKV + h.q_rows + h.kv_rows, h.qkv_rows, M, 0, s);
-    k_pf_rope_kv<T><<<M, 256, 0, s>>>(P, h.pf_QKV, p0, kc, vc);
-    const int G = h.Hq / h.Hkv, QB = 64 / G;
-    dim3 ag((M + QB - 1) / QB, h.Hkv);
-    const size_t sm = 2 * PF_KT * h.hd * sizeof(float);
-    if (h.hd == 128) k_pf_attn<T, 128><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
-    else if (h.hd == 64) k_pf_attn<T, 64><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
-    else k_pf_attn<T, 32><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
-    pf_gemm<T>(h.pf_ATT, h.q_rows, w.wo, d, h.q_rows, H, d, M, 1, s);
-    k_pf_norm<<<M, 256, 0, s>>>(H, h.pf_XN, w.g2, d, h.eps);
-    pf_gemm<T>(h.pf_XN, d, w.wg, h.F, d, h.pf_GU, 2 * h.F, M, 0, s);
-    pf_gemm<T>(h.pf_XN, d, w.wu, h.F, d, h.pf_GU + h.F, 2 * h.F, M, 0, s);
-    k_pf_silu<<<1024, 256, 0, s>>>(P, M);
-    pf_gemm<T>(h.pf_XN, h.F, w.wd, d, h.F, H, d, M, 1, s);
+// Tensor-core GEMM launch (bf16 weights): C[M][N] (+)= (A_hi + A_lo)[M][K] . W[N][K]^T with
+// A in pf_A2 (row pitch K).  The tensor maps are encoded on the host per call (a few
+// microseconds); the tile width BN is the largest of 256 / 128 / 64 that divides N and
+// still gives about one CTA per SM.
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 map over rows x K (K contiguous), box 64 (K) x box_rows, 128-byte swizzle
+static bool tmap_bf16(CUtensorMap *m, const void *base, int K, long long rows, int box_rows) {
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)UM_BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int g_num_sms = 0;
+
+template <int BN>
+static bool um_launch(const Plan &h, const void *W, int N, int K, float *C, int ldc, int M, int acc, cudaStream_t s) {
+    CUtensorMap ta, tw;
+    if (!tmap_bf16(&ta, h.pf_A2, K, 2LL * h.pf_rows, UM_BM) || !tmap_bf16(&tw, W, K, N, BN)) return false;
+    const UmmaArgs a{C, ldc, M, N, K, h.pf_rows, acc, &h.st->error};
+    k_umma_gemm<BN><<<dim3(N / BN, (M + UM_BM - 1) / UM_BM), UM_THREADS, UM_SMEM, s>>>(ta, tw, a);
+    return true;
+}
+
+static bool um_gemm(const Plan &h, const void *W, int N, int K, float *C, int ldc, int M, int acc, cudaStream_t s) {
+    const int mt = (M + UM_BM - 1) / UM_BM, want = g_num_sms > 0 ? g_num_sms : 148;
+    if (N % 256 == 0 && (N / 256) * mt >= want) return um_launch<256>(h, W, N, K, C, ldc, M, acc, s);
+    if (N % 128 == 0 && ((N / 128) * mt >= want || N % 64 != 0)) return um_launch<128>(h, W, N, K, C, ldc, M, acc, s);
+    return um_launch<64>(h, W, N, K, C, ldc, M, acc, s);
 }
 
 template <typename T>
-void launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int grid, cudaStream_t s) {
-    (void)grid;
+static bool pf_layer(const Plan *P, const Plan &h, const LayerW &w, KvT<T> *kc, KvT<T> *vc, float *H, int p0, int M,
+                     cudaStream_t s) {
+    using KV = KvT<T>;
+    constexpr bool TC = sizeof(T) == 2;   // bf16 weights: tensor-core GEMMs
+    const int d = h.d;
+    bool ok = true;
+    if (TC) {
+        k_pf_norm_split<<<M, 256, 0, s>>>(H, h.pf_A2, h.pf_rows, w.g1, d, h.eps);
+        ok = ok && um_gemm(h, w.wq, h.q_rows, d, h.pf_QKV, h.qkv_rows, M, 0, s);
+        ok = ok && um_gemm(h, w.wk, h.kv_rows, d, h.pf_QKV + h.q_rows, h.qkv_rows, M, 0, s);
+        ok = ok && um_gemm(h, w.wv, h.kv_rows, d, h.pf_QKV + h.q_rows + h.kv_rows, h.qkv_rows, M, 0, s);
+    } else {
+        k_pf_norm<<<M, 256, 0, s>>>(H, h.pf_XN, w.g1, d, h.eps);
+        pf_gemm<T>(h.pf_XN, d, w.wq, h.q_rows, d, h.pf_QKV, h.qkv_rows, M, 0, s);
+        pf_gemm<T>(h.pf_XN, d, w.wk, h.kv_rows, d, h.pf_QKV + h.q_rows, h.qkv_rows, M, 0, s);
+        pf_gemm<T>(h.pf_XN, d, w.wv, h.kv_rows, d, h.pf_QKV + h.q_rows + h.kv_rows, h.qkv_rows, M, 0, s);
+    }
+    k_pf_rope_kv<KV><<<M, 256, 0, s>>>(P, h.pf_QKV, p0, kc, vc);
+    const int G = h.Hq / h.Hkv, QB = 64 / G;
+    dim3 ag((M + QB - 1) / QB, h.Hkv);
+    const size_t sm = 2 * PF_KT * h.hd * sizeof(float);
+    if (h.hd == 128) k_pf_attn<KV, 128><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+    else k_pf_attn<KV, 64><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+    if (TC) {
+        k_pf_split<<<1024, 256, 0, s>>>(h.pf_ATT, h.q_rows, h.q_rows, M, h.pf_A2, h.pf_rows);
+        ok = ok && um_gemm(h, w.wo, d, h.q_rows, H, d, M, 1, s);
+        k_pf_norm_split<<<M, 256, 0, s>>>(H, h.pf_A2, h.pf_rows, w.g2, d, h.eps);
+        ok = ok && um_gemm(h, w.wg, h.F, d, h.pf_GU, 2 * h.F, M, 0, s);
+        ok = ok && um_gemm(h, w.wu, h.F, d, h.pf_GU + h.F, 2 * h.F, M, 0, s);
+        k_pf_silu_split<<<1024, 256, 0, s>>>(P, M);
+        ok = ok && um_gemm(h, w.wd, d, h.F, H, d, M, 1, s);
+    } else {
+        pf_gemm<T>(h.pf_ATT, h.q_rows, w.wo, d, h.q_rows, H, d, M, 1, s);
+        k_pf_norm<<<M, 256, 0, s>>>(H, h.pf_XN, w.g2, d, h.eps);
+        pf_gemm<T>(h.pf_XN, d, w.wg, h.F, d, h.pf_GU, 2 * h.F, M, 0, s);
+        pf_gemm<T>(h.pf_XN, d, w.wu, h.F, d, h.pf_GU + h.F, 2 * h.F, M, 0, s);
+        k_pf_silu<<<1024, 256, 0, s>>>(P, M);
+        pf_gemm<T>(h.pf_XN, h.F, w.wd, d, h.F, H, d, M, 1, s);
+    }
+    return ok;
+}
+
+template <typename T>
+int launch_prefill(const Plan *P, const Plan &h, const int *prompt, int prompt_len, int num_sms, cudaStream_t s) {
+    constexpr bool TC = sizeof(T) == 2;
+    g_num_sms = num_sms;
+    bool ok = true;
     for (int p0 = 0; p0 < prompt_len; p0 += h.pf_rows) {
         const int M = prompt_len - p0 < h.pf_rows ? prompt_len - p0 : h.pf_rows;
         k_pf_embed<T><<<M, 256, 0, s>>>(P, prompt, p0);
         for (int l = 0; l < h.L; ++l) {
-            T *kc = reinterpret_cast<T *>(h.kc) + (long long)l * h.kv_stride;
-            T *vc = reinterpret_cast<T *>(h.vc) + (long long)l * h.kv_stride;
-            pf_layer<T>(P, h, h.tl[l], kc, vc, h.pf_H, p0, M, s);
+            KvT<T> *kc = reinterpret_cast<KvT<T> *>(h.kc) + (long long)l * h.kv_stride;
+            KvT<T> *vc = reinterpret_cast<KvT<T> *>(h.vc) + (long long)l * h.kv_stride;
+            ok = ok && pf_layer<T>(P, h, h.tl[l], kc, vc, h.pf_H, p0, M, s);
             if (h.aidx[l + 1] >= 0) k_pf_anchor<<<512, 256, 0, s>>>(P, M, h.aidx[l + 1]);
         }
         if (h.Ls > 0) {
-            pf_gemm<T>(h.pf_ANCH, h.nB * h.d, h.proj, h.d, h.nB * h.d, h.pf_Hp, h.d, M, 0, s);
+            if (TC) {
+                const int K = h.nB * h.d;
+                k_pf_split<<<1024, 256, 0, s>>>(h.pf_ANCH, K, K, M, h.pf_A2, h.pf_rows);
+                ok = ok && um_gemm(h, h.proj, h.d, K, h.pf_Hp, h.d, M, 0, s);
+            } else {
+                pf_gemm<T>(h.pf_ANCH, h.nB * h.d, h.proj, h.d, h.nB * h.d, h.pf_Hp, h.d, M, 0, s);
+            }
             for (int l = 0; l < h.Ls; ++l) {
-                T *kc = reinterpret_cast<T *>(h.pkc) + (long long)l * h.kv_stride;
-                T *vc = reinterpret_cast<T *>(h.pvc) + (long long)l * h.kv_stride;
-                pf_layer<T>(P, h, h.pl[l], kc, vc, h.pf_Hp, p0, M, s);
+                KvT<T> *kc = reinterpret_cast<KvT<T> *>(h.pkc) + (long long)l * h.kv_stride;
+                KvT<T> *vc = reinterpret_cast<KvT<T> *>(h.pvc) + (long long)l * h.kv_stride;
+                ok = ok && pf_layer<T>(P, h, h.pl[l], kc, vc, h.pf_Hp, p0, M, s);
             }
         }
         if (p0 + M == prompt_len)
             k_pf_logits<T><<<1024, 256, h.d * sizeof(float), s>>>(P, h.pf_H + (long long)(M - 1) * h.d);
+        if (!ok) return 1;
     }
     launch_prefill_finalize<T>(P, prompt_len, s);
+    return 0;
 }
 
 __global__ void k_rope_table(float2 *tab, int max_seq, int half, int hd, double theta) {
@@ -331,12 +456,15 @@ void launch_rope_table(const Plan &h, float theta, cudaStream_t s) {
 
 void set_prefill_attributes() {
     cudaFuncSetAttribute(k_pf_attn<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
-    cudaFuncSetAttribute(k_pf_attn<__nv_bfloat16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
+    cudaFuncSetAttribute(k_pf_attn<KvT<__nv_bfloat16>, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
     cudaFuncSetAttribute(k_pf_logits<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     cudaFuncSetAttribute(k_pf_logits<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(k_umma_gemm<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
+    cudaFuncSetAttribute(k_umma_gemm<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
+    cudaFuncSetAttribute(k_umma_gemm<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
 }
 
-template void launch_prefill<float>(const Plan *, const Plan &, const int *, int, int, cudaStream_t);
-template void launch_prefill<__nv_bfloat16>(const Plan *, const Plan &, const int *, int, int, cudaStream_t);
+template int launch_prefill<float>(const Plan *, const Plan &, const int *, int, int, cudaStream_t);
+template int launch_prefill<__nv_bfloat16>(const Plan *, const Plan &, const int *, int, int, cudaStream_t);
 
 }  // namespace spd

@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
             if (lane == 0) {
                 s_done = st->done;
                 s_rows[0] = (mask >> (n - 1)) & 1u ? ring(head, n - 1, ns) : -1;
-                s_rows[1] = (st->pending ? 1 : 0) + __popc(mask) - 1;
+                s_rows[1] = (pdm_pending(P, st) ? 1 : 0) + __popc(mask) - 1;
                 SL.m = 1;
                 SL.stage[0] = SL.slot[0] = SL.layer[0] = 0;
             }
@@ -406,8 +406,15 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                         const int kc0 = c * KC, len = min(KC, K - kc0);
                         const int sidx = tile % NS;
                         const uint32_t u = tile / NS;
-                        if (!mbar_wait(&empty[sidx], (u & 1) ^ 1)) P->st->error = ERR_TIMEOUT;
+                        if (!mbar_wait(&empty[sidx], (u & 1) ^ 1, P->wait_cycles)) P->st->error = ERR_TIMEOUT;
                         const uint32_t bytes = (uint32_t)len * sizeof(T);
+                        // test hook (off unless the handle was created with it): the CTA's very
+                        // last tile is never loaded, so its consumers' wait runs out
+                        if (EPI == EPI_GATEUP && P->test_withhold && blockIdx.x == 0 && round == 0 && c == nch - 1 &&
+                            g == per - 1 && (long long)(i + 1) * N >= hi && P->st->t == 0) {
+                            ++tile;
+                            continue;
+                        }
                         mbar_expect_tx(&full[sidx], bytes * nrows);
 #pragma unroll
                         for (int q = 0; q < TG_RG; ++q)
@@ -473,8 +480,8 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                     const int uA = slot_unit(r0, per, GR, q, g), uB = slot_unit(r0, per, GR, q, g + 1);
                     const bool rvA = uA < r1, rvB = two && uB < r1;
                     const int sA = tile % NS, sB = (tile + 1) % NS;
-                    if (!mbar_wait(&full[sA], (tile / NS) & 1)) P->st->error = ERR_TIMEOUT;
-                    if (two && !mbar_wait(&full[sB], ((tile + 1) / NS) & 1)) P->st->error = ERR_TIMEOUT;
+                    if (!mbar_wait(&full[sA], (tile / NS) & 1, P->wait_cycles)) P->st->error = ERR_TIMEOUT;
+                    if (two && !mbar_wait(&full[sB], ((tile + 1) / NS) & 1, P->wait_cycles)) P->st->error = ERR_TIMEOUT;
                     const unsigned char *tA = stages + sA * stage_bytes + q * rowb;
                     const unsigned char *tB = stages + sB * stage_bytes + q * rowb;
                     float cA = 0.f, eA = 0.f, cB = 0.f, eB = 0.f;
@@ -544,7 +551,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                 const int kc0 = c * KC, len = min(KC, K - kc0);
                 const int sidx = tile % NS;
                 const uint32_t u = tile / NS;
-                if (!mbar_wait(&full[sidx], u & 1)) P->st->error = ERR_TIMEOUT;
+                if (!mbar_wait(&full[sidx], u & 1, P->wait_cycles)) P->st->error = ERR_TIMEOUT;
                 if (rv) {
                     const unsigned char *tb = stages + sidx * stage_bytes + q * rowb;
                     const int nvec = len / VEC;
@@ -598,7 +605,13 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                         P->ANCH[((long long)slot * P->nB + a) * d + unit] = xn;
                         if (sizeof(T) == 2) P->ANCHb[((long long)slot * P->nB + a) * d + unit] = __float2bfloat16_rn(xn);
                     }
-                    if (lm_row) P->Xlm[unit] = __float2bfloat16_rn(xn * gfin);
+                    if (lm_row) {
+                        // the LM head's input row in two bf16 parts: the value and the rest
+                        const float xl = xn * gfin;
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(xl);
+                        P->Xlm[unit] = hi;
+                        P->Xlm[2 * d + unit] = __float2bfloat16_rn(xl - __bfloat162float(hi));
+                    }
                 } else {
                     // logits: tied -> both rows of this vocab id; untied -> row (q >= 4) only
                     const int h0 = TIED ? 0 : (q < 4 ? 0 : 1);

@@ -264,9 +264,9 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
             const float a = first ? v : partner, b = first ? partner : v;
             const float y = first ? a * cs.x - b * cs.y : b * cs.x + a * cs.y;
             if (row < P->q_rows) P->QKVp[(long long)xr * P->qkv_rows + row] = y;
-            else reinterpret_cast<T *>(P->pkc)[cache + (row - P->q_rows)] = WTraits<T>::store(y);
+            else reinterpret_cast<KvT<T> *>(P->pkc)[cache + (row - P->q_rows)] = WTraits<KvT<T>>::store(y);
         } else {
-            reinterpret_cast<T *>(P->pvc)[cache + (row - P->q_rows - P->kv_rows)] = WTraits<T>::store(v);
+            reinterpret_cast<KvT<T> *>(P->pvc)[cache + (row - P->q_rows - P->kv_rows)] = WTraits<KvT<T>>::store(v);
         }
     } else if (OP == OP_GATEUP) {
         // slots 0-3 hold gate rows u, slots 4-7 the up rows F + u, in lane ^ 2 (thread bit 3)
@@ -285,7 +285,13 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
             // the newest row is the LM head's second input row
             if (sizeof(T) == 2) {
                 if (OP != OP_DOWN || layer + 1 < P->Ls) P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * pre.y);
-                else if (xr == pr.R - 1) P->Xlm[P->d + row] = __float2bfloat16_rn(o * pre.y);
+                else if (xr == pr.R - 1) {
+                    // the LM head's second input row in two bf16 parts: the value and the rest
+                    const float xl = o * pre.y;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(xl);
+                    P->Xlm[P->d + row] = hi;
+                    P->Xlm[3 * P->d + row] = __float2bfloat16_rn(xl - __bfloat162float(hi));
+                }
             }
         }
         // sum of squares of the 8 rows of this group for x row xr (lanes differing in thread
@@ -438,8 +444,10 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     const int N = pg_N<OP>(*P), K = pg_K<OP>(*P), G8 = N / 8;
     const int nb = m_pdm / ns, b = p / ns, sl = p - (p / ns) * ns;
     if (b >= nb || (OP != OP_LM && pr.R < 1)) return;
-    // LM head: row 0 = the token leaving the last stage, row 1 = the draft module's newest row
-    const int R = OP == OP_LM ? 2 : pr.R;
+    // LM head: rows 0, 1 = the token leaving the last stage and the draft module's newest row
+    // (bf16 of x * g_final), rows 2, 3 = bf16 of what rows 0, 1 left out of x * g_final; the
+    // products of rows r and r + 2 are added, so the head sees x at about 16 mantissa bits
+    const int R = OP == OP_LM ? 4 : pr.R;
     const int k0 = sl * kx, kw = min(kx, K - k0);
     const int gb0 = (int)((long long)G8 * b / nb), gb1 = (int)((long long)G8 * (b + 1) / nb);
     const int nch = pg_nch(kw, ESZ), KC = pg_kc(kw, ESZ);
@@ -450,7 +458,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // bulk copies (the projection's per anchor, masked ones zeroed instead); the
     // register-resident fragments are then read from there
     constexpr bool BULK = ESZ == 2;
-    const int xbytes = pg_xbytes(OP == OP_LM ? 2 : P->n + 1, kx, ESZ);
+    const int xbytes = pg_xbytes(OP == OP_LM ? 4 : P->n + 1, kx, ESZ);
     unsigned char *xs = smem;
     float4 *red = reinterpret_cast<float4 *>(smem + xbytes);
     unsigned char *stages = smem + xbytes + pg_redbytes(MT);
@@ -670,7 +678,12 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
             const int row = wrows.row_of(g, wr_t);
             if constexpr (OP == OP_LM) {
                 if (xr_t < 2) {
-                    const float z = s * s_inv[xr_t];
+                    // x row xr_t + 2 (the remainder part) sits 8 fragment lanes further
+                    float lo = 0.f;
+#pragma unroll
+                    for (int w = 0; w < PG_CONSUMERS / 32; ++w)
+                        lo += rf[(((buf * (PG_CONSUMERS / 32) + w) * MT + rm) * 32 + rl + 8) * 4 + rreg];
+                    const float z = (s + lo) * s_inv[xr_t];
                     P->logits[(long long)xr_t * N + row] = z;
                     if (xr_t == 1 && dl) dl[row] = z;
                     if (z > lbv || (z == lbv && row < lbi)) {

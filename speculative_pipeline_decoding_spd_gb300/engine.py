@@ -33,7 +33,8 @@ class Engine:
     def __init__(self, dims, target: Dict, pdm: Optional[Dict], n: int, anchors: Sequence[int], *,
                  max_seq: int, max_new: int, temperature: float = 0.0, seed: int = 2, force_p: float = -1.0,
                  forced_ref: Optional[torch.Tensor] = None, graph: bool = True, timing: bool = False,
-                 stream: Optional[torch.cuda.Stream] = None, workspace_fill: Optional[int] = None):
+                 stream: Optional[torch.cuda.Stream] = None, workspace_fill: Optional[int] = None,
+                 bounds: Optional[Sequence[int]] = None, speculate: str = "input"):
         self.dims = dims
         self.n = n
         self.max_new = max_new
@@ -58,6 +59,10 @@ class Engine:
         self.cfg = B.spd_config(n, len(anchors), a, float(temperature), int(seed), int(max_seq), int(max_new),
                                 float(force_p), forced_ref.data_ptr() if forced_ref is not None else None,
                                 int(forced_ref.numel()) if forced_ref is not None else 0, int(graph), int(timing))
+        if bounds is not None:
+            for i, v in enumerate(bounds):
+                self.cfg.stage_bounds[i] = int(v)
+        self.cfg.speculate = {"input": B.SPD_SPEC_INPUT, "output": B.SPD_SPEC_OUTPUT}[speculate]
         self.ws_bytes = B.spd_workspace_bytes(self.cd, self.pw, self.cfg)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
         if workspace_fill is not None:   # tests: the library must not rely on zeroed memory

@@ -38,3 +38,23 @@ def test_traffic_file_is_a_per_stage_layer_figure():
     # DRAM bytes of one stage-layer of gate/up: its weights once, plus the small outputs
     alg = 2 * si.SHAPE_4B.dims.F * si.SHAPE_4B.dims.d * 2
     assert alg * 0.99 < tj["dram_bytes_per_stage_layer"] < alg * 1.05
+
+
+def test_alpha_ref_is_the_closed_form_or_one_over_n():
+    assert bench.alpha_ref("forced-0.6", 8) == 1.0 / (1.0 + 7 * 0.4)
+    assert bench.alpha_ref("forced-1.0", 8) == 1.0
+    assert bench.alpha_ref("greedy", 8) == 1.0 / 8
+    assert bench.alpha_ref("t1", 8) is None
+    assert bench.cpu_alpha("t1", 8, 0.31) == 0.31
+    assert bench.cpu_alpha("forced-0.3", 8, 0.5) == 1.0 / (1.0 + 7 * 0.7)
+
+
+def test_workload_selection():
+    class A:
+        mode, shape, n = "forced-0.6", "4b", 0
+    assert bench.select_workload(A) is si.SHAPE_4B
+    A.mode = "t1"
+    assert bench.select_workload(A) is si.SHAPE_4B_T1
+    A.mode, A.shape, A.n = "forced-0.7", "8b", 16
+    wl = bench.select_workload(A)
+    assert wl.dims == si.SHAPE_8B.dims and wl.n == 16 and wl.prompt_len == 4096 and wl.Ls == 2

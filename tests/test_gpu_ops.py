@@ -1,10 +1,9 @@
 """GPU parity of the standalone decode attention (spd_attention_decode) against the oracle.
 
-Shapes cover GQA groups 1..8, both head dims, fp32 and bf16 caches, and sequence lengths
-of one chunk, exact chunk multiples and ragged tails over several 128-position chunks.
-Tolerance: rel 1e-4 (fp32 cache) / 2e-2 (bf16 cache) of max |out|; the bf16 case feeds
-the oracle the same bf16-rounded K and V, so its error is fp32 rounding only and the
-test also checks it against 1e-4."""
+Shapes cover GQA groups 1..8, both head dims, fp32, bf16 and fp16 caches, and sequence
+lengths of one chunk, exact chunk multiples and ragged tails over several 128-position
+chunks.  The oracle gets the same rounded K and V, so every case's error is fp32
+rounding only: rel 1e-4 of max |out|."""
 import numpy as np
 import pytest
 import torch
@@ -22,6 +21,8 @@ def _case(Hq, Hkv, hd, S, dtype, seed):
     v = torch.randn(S, Hkv, hd, generator=g)
     if dtype == B.SPD_BF16:
         k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    elif dtype == B.SPD_F16:
+        k, v = k.to(torch.float16), v.to(torch.float16)
     return q, k, v
 
 
@@ -40,7 +41,7 @@ def run_attention(q, k, v, dtype):
 
 @pytest.mark.parametrize("Hq,Hkv,hd", [(4, 4, 64), (8, 4, 64), (32, 8, 128), (16, 2, 128)])
 @pytest.mark.parametrize("S", [1, 77, 128, 129, 300, 1025])
-@pytest.mark.parametrize("dtype", [B.SPD_F32, B.SPD_BF16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("dtype", [B.SPD_F32, B.SPD_BF16, B.SPD_F16], ids=["f32", "bf16", "f16"])
 def test_attention_matches_oracle(Hq, Hkv, hd, S, dtype):
     q, k, v = _case(Hq, Hkv, hd, S, dtype, seed=S * 7 + Hq)
     got = run_attention(q, k, v, dtype)

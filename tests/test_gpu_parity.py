@@ -11,7 +11,9 @@ import pytest
 import torch
 
 import spd_inputs as si
-from gpu_common import Case, ar_reference, compare, engine, materialise, replay_oracle, run_gpu
+from gpu_common import (Case, ar_reference, compare, engine, materialise, replay_oracle, run_gpu,
+                        step_and_compare_vectors)
+from oracle import Replay, SPDOracle
 
 pytestmark = pytest.mark.gpu
 
@@ -179,3 +181,102 @@ def test_untied_head_copy_replay():
     o, rep = replay_oracle(case, tr, toks)
     compare(case, tr, o, rep)
     assert o.tokens[case.prompt_len:] == toks
+
+
+# ---- vectors, step by step --------------------------------------------------------------
+
+VEC_CASES = [
+    ("tiny", TINY, {}),
+    ("small", SMALL, {}),
+    ("small-forced", SMALL, dict(p=0.6)),
+    ("hd128-forced", HD128, dict(p=0.6)),
+    ("multi", MULTI, {}),
+    ("wide-forced", WIDE, dict(p=0.7)),
+    ("widek", WIDEK, {}),
+    ("inrounds-forced", INROUNDS, dict(p=0.6)),
+    ("small-output", SMALL, dict(speculate="output", p=0.6)),
+    ("hd128-bounds", HD128, dict(bounds=(0, 1, 2, 4, 5), p=0.6)),
+]
+
+
+def vector_run(case, steps, p=None, speculate="input", bounds=None, n=None):
+    """Prefill both sides, then compare the vectors after each of `steps` steps."""
+    tg, pd, prompt, m, _, _ = materialise(case)
+    n = n or case.n
+    kw = dict(speculate=speculate, bounds=bounds)
+    okw = dict(speculate=speculate, bounds=bounds)
+    if p is not None:
+        ref = np.array(list(prompt) + ar_reference(case) + [0] * (case.n + 8), dtype=np.int32)
+        kw.update(force_p=p, forced_ref=torch.from_numpy(ref).cuda(), seed=5)
+        okw.update(forced_p=p, forced_ref=ref, seed=5)
+    e = engine(case, n=n, graph=False, **kw)
+    e.prefill(torch.from_numpy(prompt).cuda())
+    y0 = e.tokens()[0]
+    o = SPDOracle(m, n, case.max_seq, replay=Replay(steps={}, prefill_y0=y0, tol=case.tol), **okw)
+    o.prefill(prompt)
+    worst = step_and_compare_vectors(case, e, o, steps)
+    e.close()
+    return worst, o
+
+
+@pytest.mark.parametrize("name,case,kw", VEC_CASES, ids=[c[0] for c in VEC_CASES])
+def test_vectors_match_oracle_step_by_step(name, case, kw):
+    """Logits entry by entry, the draft block's residual rows, every in-flight residual
+    stream and anchor state, and the K/V rows each step writes, against the oracle after
+    each of the first 12 steps, all within the case's one tolerance."""
+    worst, o = vector_run(case, 12, **kw)
+    if kw.get("p") is not None:
+        assert any(r["accept"] == 0 for r in o.trace)     # a rollback happened inside the window
+
+
+# ---- the output-state schedule and non-uniform stages -----------------------------------
+
+@pytest.mark.parametrize("case,p", [(SMALL, None), (SMALL, 0.6), (HD128, 0.7), (WIDE, 0.8), (TINY, 0.6)],
+                         ids=["small", "small-0.6", "hd128-0.7", "wide-0.8", "tiny-0.6"])
+def test_output_state_schedule_replay(case, p):
+    """The draft module after the step, on its output states (stage s at depth b_{s+1}):
+    the whole run replayed against the oracle's output-state simulator; the committed
+    tokens are the same as under the input-state schedule."""
+    kw, okw = {}, {}
+    if p is not None:
+        tg, pd, prompt, m, _, _ = materialise(case)
+        ref = np.array(list(prompt) + ar_reference(case) + [0] * (case.n + 8), dtype=np.int32)
+        kw = dict(force_p=p, forced_ref=torch.from_numpy(ref).cuda(), seed=5)
+        okw = dict(forced_p=p, forced_ref=ref, seed=5)
+    toks, tr, st, pf = run_gpu(case, speculate="output", **kw)
+    o, rep = replay_oracle(case, tr, toks, speculate="output", **okw)
+    compare(case, tr, o, rep)
+    assert o.tokens[case.prompt_len:] == toks
+    if p is None:
+        # the schedules' draft modules see different features
+        toks_in, tr_in, _, _ = run_gpu(case)
+        assert toks_in == toks
+        assert [r["pdm_logit"] for r in tr_in] != [r["pdm_logit"] for r in tr]
+
+
+@pytest.mark.parametrize("case,bounds,p", [(SMALL, (0, 1, 5, 6), None), (SMALL, (0, 4, 5, 6), 0.6),
+                                           (HD128, (0, 3, 4, 5), 0.7), (WIDE, tuple(range(0, 33, 2)), 0.8),
+                                           (MULTI, (0, 1, 4), 0.6)],
+                         ids=["small-1-4-1", "small-4-1-1", "hd128-3-1-1", "wide-uniform", "multi-1-3"])
+def test_non_uniform_stages_replay(case, bounds, p):
+    """Explicit stage partitions (the referee report's Appendix C.1 comment): the whole run
+    replayed against the oracle with the same bounds; per-layer KV lengths follow them."""
+    n = len(bounds) - 1
+    kw, okw = {}, {}
+    if p is not None:
+        tg, pd, prompt, m, _, _ = materialise(case)
+        ref = np.array(list(prompt) + ar_reference(case) + [0] * (n + 8), dtype=np.int32)
+        kw = dict(force_p=p, forced_ref=torch.from_numpy(ref).cuda(), seed=5)
+        okw = dict(forced_p=p, forced_ref=ref, seed=5)
+    toks, tr, st, pf = run_gpu(case, n=n, bounds=bounds, **kw)
+    o, rep = replay_oracle(case, tr, toks, n=n, bounds=bounds, **okw)
+    compare(case, tr, o, rep)
+    assert o.tokens[case.prompt_len:] == toks
+
+
+def test_bad_stage_bounds_are_refused():
+    from speculative_pipeline_decoding_spd_gb300 import binding as B
+    for bounds in [(0, 3, 3, 6), (1, 3, 6), (0, 2, 5)]:
+        with pytest.raises(B.SPDError) as e:
+            engine(SMALL, n=len(bounds) - 1, bounds=bounds)
+        assert e.value.code == B.SPD_EINVAL
