@@ -8,8 +8,9 @@
 // the cache of the chunks before it).  bf16 weights: every projection is a tensor-core
 // GEMM (umma.cuh: tcgen05, TMEM accumulators, TMA-fed operands) whose activation operand
 // comes as two bf16 parts written by the kernel before it (the norm, the attention
-// output's split, SiLU(gate) * up, the anchors' split).  fp32 weights: an fp32 tiled
-// CUDA-core GEMM.  The causal attention stages K/V tiles in shared memory.
+// output's split, SiLU(gate) * up, the anchors' split), and the causal attention runs on
+// tensor cores too (mma.sync over the fp16 K/V cache, flash-attention order).  fp32
+// weights: an fp32 tiled CUDA-core GEMM and attention.
 #include <cudaTypedefs.h>
 
 #include <string>
@@ -232,6 +233,205 @@ __global__ void __launch_bounds__(256) k_pf_attn(const Plan *__restrict__ P, con
     }
 }
 
+// ---- causal attention of a prompt chunk on tensor cores (fp16 K/V cache) ------------------
+// CTA = 64 query rows of one query head (4 warps x 16 rows), flash-attention order: key
+// tiles of 64 positions staged in shared memory by cp.async (double buffered), scores
+// S = Q K^T by mma.sync m16n8k16 (q as two fp16 parts, hi and lo, so the scores see about
+// 21 bits of q; K as stored), an online softmax per row in registers, P rounded to fp16 and
+// O += P V by mma.sync; the causal mask applies on the diagonal tile only.  Output fp32
+// [row][Hq * hd], as the tensor-core O projection's input split expects.
+constexpr int FA_BQ = 64, FA_BK = 64, FA_THREADS = 128;
+template <int HD> __host__ __device__ constexpr int fa_pitch() { return HD + 8; }   // halfs; ldmatrix rows on distinct banks
+template <int HD> __host__ __device__ constexpr int fa_smem_bytes() {
+    return (2 * FA_BQ + 4 * FA_BK) * fa_pitch<HD>() * 2;   // q hi, q lo, two stages of K and V
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P, const float *__restrict__ qkv, int p0,
+                                                      int M, const __half *__restrict__ kc, const __half *__restrict__ vc,
+                                                      float *__restrict__ out) {
+    extern __shared__ __align__(16) __half fa_s[];
+    constexpr int PT = fa_pitch<HD>(), NT = FA_BK / 8, KS = HD / 16, NO = HD / 8;
+    __half *Qh = fa_s, *Ql = Qh + FA_BQ * PT, *Ks = Ql + FA_BQ * PT, *Vs = Ks + 2 * FA_BK * PT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+    const int h = blockIdx.y, G = P->Hq / P->Hkv, g = h / G;
+    const int q0 = blockIdx.x * FA_BQ;
+    const long long rs = (long long)P->Hkv * HD;
+    const int kv_end = p0 + M;                                  // keys written so far
+    const int kend = min(kv_end, p0 + q0 + FA_BQ);              // keys any row of this CTA sees
+    const int ntiles = (kend + FA_BK - 1) / FA_BK;
+    const float scale = P->scale;
+    // ---- K / V tile loader (rows past the written keys are zero)
+    auto load_tile = [&](int t, int buf) {
+        const int k0 = t * FA_BK;
+        for (int c = tid; c < FA_BK * HD / 8; c += FA_THREADS) {
+            const int j = c / (HD / 8), e = (c - j * (HD / 8)) * 8;
+            __half *kd = Ks + (buf * FA_BK + j) * PT + e;
+            __half *vd = Vs + (buf * FA_BK + j) * PT + e;
+            if (k0 + j < kv_end) {
+                cp_async16(kd, kc + (long long)(k0 + j) * rs + (long long)g * HD + e);
+                cp_async16(vd, vc + (long long)(k0 + j) * rs + (long long)g * HD + e);
+            } else {
+                *reinterpret_cast<uint4 *>(kd) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(vd) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load_tile(0, 0);
+    // ---- q (rotated already), pre-scaled by 1/sqrt(hd), as fp16 hi + lo
+    for (int c = tid; c < FA_BQ * HD; c += FA_THREADS) {
+        const int r = c / HD, e = c - r * HD;
+        const int m = min(q0 + r, M - 1);
+        const float v = qkv[(long long)m * P->qkv_rows + (long long)h * HD + e] * scale;
+        const __half hi = __float2half_rn(v);
+        Qh[r * PT + e] = hi;
+        Ql[r * PT + e] = __float2half_rn(v - __half2float(hi));
+    }
+    float o[NO][4];
+#pragma unroll
+    for (int i = 0; i < NO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    const int r0 = warp * 16;                                   // this warp's first row in the tile
+    const int qpos0 = p0 + q0 + r0 + gq, qpos1 = qpos0 + 8;      // positions of the thread's two rows
+    const uint32_t qh_addr = smem_u32(Qh + (r0 + (lane & 15)) * PT + (lane >> 4) * 8);
+    const uint32_t ql_addr = smem_u32(Ql + (r0 + (lane & 15)) * PT + (lane >> 4) * 8);
+    for (int t = 0; t < ntiles; ++t) {
+        const int buf = t & 1;
+        if (t + 1 < ntiles) {
+            load_tile(t + 1, buf ^ 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        // ---- S = Q K^T: 16 rows x 64 keys per warp
+        float sc[NT][4];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+        const __half *kb = Ks + buf * FA_BK * PT;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3;
+            ldsm_x4(qh_addr + ks * 32, ah0, ah1, ah2, ah3);
+            ldsm_x4(ql_addr + ks * 32, al0, al1, al2, al3);
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np) {
+                // keys 16 np .. 16 np + 15: two n8 tiles
+                uint32_t b0, b1, b2, b3;
+                const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                ldsm_x4(smem_u32(kb + key * PT + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1, b2, b3);
+                mma_f16(sc[2 * np], ah0, ah1, ah2, ah3, b0, b1);
+                mma_f16(sc[2 * np], al0, al1, al2, al3, b0, b1);
+                mma_f16(sc[2 * np + 1], ah0, ah1, ah2, ah3, b2, b3);
+                mma_f16(sc[2 * np + 1], al0, al1, al2, al3, b2, b3);
+            }
+        }
+        // ---- causal mask on the diagonal tile, online softmax
+        const int k0 = t * FA_BK;
+        if (k0 + FA_BK - 1 > qpos0) {
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                const int key = k0 + i * 8 + 2 * tq;
+                if (key > qpos0) sc[i][0] = -INFINITY;
+                if (key + 1 > qpos0) sc[i][1] = -INFINITY;
+                if (key > qpos1) sc[i][2] = -INFINITY;
+                if (key + 1 > qpos1) sc[i][3] = -INFINITY;
+            }
+        }
+        float mx[2] = {mrow[0], mrow[1]};
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            mx[0] = fmaxf(mx[0], fmaxf(sc[i][0], sc[i][1]));
+            mx[1] = fmaxf(mx[1], fmaxf(sc[i][2], sc[i][3]));
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        }
+        float corr[2], ls[2] = {0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) corr[r] = mx[r] == -INFINITY ? 1.f : expf(mrow[r] - mx[r]);
+        uint32_t pa[NT][2];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            const float e0 = mx[0] == -INFINITY ? 0.f : expf(sc[i][0] - mx[0]);
+            const float e1 = mx[0] == -INFINITY ? 0.f : expf(sc[i][1] - mx[0]);
+            const float e2 = mx[1] == -INFINITY ? 0.f : expf(sc[i][2] - mx[1]);
+            const float e3 = mx[1] == -INFINITY ? 0.f : expf(sc[i][3] - mx[1]);
+            // the row sums take the probabilities as rounded for the P V product
+            const uint32_t p01 = pack_h2(e0, e1), p23 = pack_h2(e2, e3);
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&p01));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&p23));
+            ls[0] += f01.x + f01.y;
+            ls[1] += f23.x + f23.y;
+            pa[i][0] = p01;
+            pa[i][1] = p23;
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            ls[r] += __shfl_xor_sync(0xffffffffu, ls[r], 1);
+            ls[r] += __shfl_xor_sync(0xffffffffu, ls[r], 2);
+            lrow[r] = lrow[r] * corr[r] + ls[r];
+            mrow[r] = mx[r];
+        }
+#pragma unroll
+        for (int i = 0; i < NO; ++i) {
+            o[i][0] *= corr[0];
+            o[i][1] *= corr[0];
+            o[i][2] *= corr[1];
+            o[i][3] *= corr[1];
+        }
+        // ---- O += P V
+        const __half *vb = Vs + buf * FA_BK * PT;
+#pragma unroll
+        for (int s = 0; s < FA_BK / 16; ++s) {
+            const uint32_t a0 = pa[2 * s][0], a1 = pa[2 * s][1], a2 = pa[2 * s + 1][0], a3 = pa[2 * s + 1][1];
+#pragma unroll
+            for (int np = 0; np < NO / 2; ++np) {
+                uint32_t b0, b1, b2, b3;
+                const int key = s * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                ldsm_x4_t(smem_u32(vb + key * PT + np * 16 + (lane >> 4) * 8), b0, b1, b2, b3);
+                mma_f16(o[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_f16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncthreads();   // the buffer is refilled next iteration
+    }
+    // ---- normalise and store the warp's rows
+    const int m_a = q0 + r0 + gq, m_b = m_a + 8;
+    const float inv0 = 1.0f / lrow[0], inv1 = 1.0f / lrow[1];
+#pragma unroll
+    for (int i = 0; i < NO; ++i) {
+        const int e = i * 8 + 2 * tq;
+        if (m_a < M) *reinterpret_cast<float2 *>(out + (long long)m_a * P->q_rows + (long long)h * HD + e) =
+                         make_float2(o[i][0] * inv0, o[i][1] * inv0);
+        if (m_b < M) *reinterpret_cast<float2 *>(out + (long long)m_b * P->q_rows + (long long)h * HD + e) =
+                         make_float2(o[i][2] * inv1, o[i][3] * inv1);
+    }
+}
+
 // ---- the tensor-core GEMMs' activation operand: two bf16 parts per value ------------------
 __device__ __forceinline__ void split_store(__nv_bfloat16 *A2, long long lo_off, long long i, float v) {
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
@@ -380,11 +580,18 @@ static bool pf_layer(const Plan *P, const Plan &h, const LayerW &w, KvT<T> *kc, 
         pf_gemm<T>(h.pf_XN, d, w.wv, h.kv_rows, d, h.pf_QKV + h.q_rows + h.kv_rows, h.qkv_rows, M, 0, s);
     }
     k_pf_rope_kv<KV><<<M, 256, 0, s>>>(P, h.pf_QKV, p0, kc, vc);
-    const int G = h.Hq / h.Hkv, QB = 64 / G;
-    dim3 ag((M + QB - 1) / QB, h.Hkv);
-    const size_t sm = 2 * PF_KT * h.hd * sizeof(float);
-    if (h.hd == 128) k_pf_attn<KV, 128><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
-    else k_pf_attn<KV, 64><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+    if constexpr (TC) {
+        const dim3 fg((M + FA_BQ - 1) / FA_BQ, h.Hq);
+        const __half *kh = reinterpret_cast<const __half *>(kc), *vh = reinterpret_cast<const __half *>(vc);
+        if (h.hd == 128) k_pf_fa<128><<<fg, FA_THREADS, fa_smem_bytes<128>(), s>>>(P, h.pf_QKV, p0, M, kh, vh, h.pf_ATT);
+        else k_pf_fa<64><<<fg, FA_THREADS, fa_smem_bytes<64>(), s>>>(P, h.pf_QKV, p0, M, kh, vh, h.pf_ATT);
+    } else {
+        const int G = h.Hq / h.Hkv, QB = 64 / G;
+        dim3 ag((M + QB - 1) / QB, h.Hkv);
+        const size_t sm = 2 * PF_KT * h.hd * sizeof(float);
+        if (h.hd == 128) k_pf_attn<KV, 128><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+        else k_pf_attn<KV, 64><<<ag, 256, sm, s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+    }
     if (TC) {
         k_pf_split<<<1024, 256, 0, s>>>(h.pf_ATT, h.q_rows, h.q_rows, M, h.pf_A2, h.pf_rows);
         ok = ok && um_gemm(h, w.wo, d, h.q_rows, H, d, M, 1, s);
@@ -459,6 +666,8 @@ void set_prefill_attributes() {
     cudaFuncSetAttribute(k_pf_attn<KvT<__nv_bfloat16>, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
     cudaFuncSetAttribute(k_pf_logits<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     cudaFuncSetAttribute(k_pf_logits<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(k_pf_fa<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, fa_smem_bytes<128>());
+    cudaFuncSetAttribute(k_pf_fa<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, fa_smem_bytes<64>());
     cudaFuncSetAttribute(k_umma_gemm<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
     cudaFuncSetAttribute(k_umma_gemm<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);
     cudaFuncSetAttribute(k_umma_gemm<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, UM_SMEM);

@@ -603,7 +603,13 @@ __global__ void __launch_bounds__(TG_THREADS, 1) k_gemv(const Plan *__restrict__
                     const int a = P->aidx[layer + 1];
                     if (a >= 0) {
                         P->ANCH[((long long)slot * P->nB + a) * d + unit] = xn;
-                        if (sizeof(T) == 2) P->ANCHb[((long long)slot * P->nB + a) * d + unit] = __float2bfloat16_rn(xn);
+                        if (sizeof(T) == 2) {
+                            // the draft projection's input in two bf16 parts (value, remainder)
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(xn);
+                            const long long ai = ((long long)slot * P->nB + a) * d + unit;
+                            P->ANCHb[ai] = hb;
+                            P->ANCHb[(long long)(P->n + 1) * P->nB * d + ai] = __float2bfloat16_rn(xn - __bfloat162float(hb));
+                        }
                     }
                     if (lm_row) {
                         // the LM head's input row in two bf16 parts: the value and the rest

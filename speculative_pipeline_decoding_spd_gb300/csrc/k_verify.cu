@@ -90,11 +90,15 @@ __device__ void embed_into_slot(const Plan *__restrict__ P, int slot, int tok) {
     float *x = P->X + (long long)slot * d;
     float *a0 = P->ANCH + (long long)slot * P->nB * d;
     __nv_bfloat16 *b0 = P->ANCHb + (long long)slot * P->nB * d;
+    const long long blo = (long long)(P->n + 1) * P->nB * d;   // lo parts (zero: an embedding row is bf16)
     for (int k = threadIdx.x; k < d; k += blockDim.x) {
         const float v = WTraits<T>::get(e, k);
         x[k] = v;
         a0[k] = v;
-        if (sizeof(T) == 2) b0[k] = __float2bfloat16_rn(v);
+        if (sizeof(T) == 2) {
+            b0[k] = __float2bfloat16_rn(v);
+            b0[blo + k] = __float2bfloat16_rn(0.f);
+        }
     }
 }
 

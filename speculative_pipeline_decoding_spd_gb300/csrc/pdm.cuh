@@ -8,8 +8,10 @@
 // tokens, at consecutive positions.
 //
 // Every GEMM here multiplies one weight matrix W [N][K] by R <= n+1 row vectors x [R][K]
-// (far more bytes of W than of x: bound by streaming W once from HBM).  A group of CTAs
-// does one GEMM; per CTA:
+// (far more bytes of W than of x: bound by streaming W once from HBM).  With bf16 weights
+// each x row arrives as two bf16 rows, hi = bf16(x) and lo = bf16(x - hi), and both meet the
+// weights on the tensor cores (the products add up in the same accumulators), so the
+// GEMM sees x at about 16 mantissa bits, not 8.  A group of CTAs does one GEMM; per CTA:
 //   * a producer warp streams 8-row tiles of W (each row piece up to 6 KB, 1-D bulk
 //     copies) into a shared-memory ring signalled by mbarriers;
 //   * the R rows of x for the CTA's K slab go to shared memory: for bf16 weights the kernel
@@ -49,7 +51,7 @@ constexpr int PG_RG = 8;                       // weight rows per tile (the mma'
 constexpr int PG_ROWB = 6144;                  // bytes of one row per tile piece, at most
 constexpr int PG_MAXNS = 8;                    // ring stages at most
 constexpr int PG_SMEM = 224 * 1024;            // x + reduction buffers + ring
-constexpr int PG_XMAX = 48 * 1024;             // budget of the x rows of one slab
+constexpr int PG_XMAX = 96 * 1024;             // budget of the x rows (both parts) of one slab
 constexpr int PG_XRB = 10;                     // register-resident x: 32-element blocks per warp, at most
 constexpr int PG_KB = 32;                      // K elements per warp block
 constexpr int PG_BAR = 1;                      // named barrier of the consumer warps
@@ -133,6 +135,13 @@ __device__ __forceinline__ PgRows<T, OP> pg_rows(const Plan *__restrict__ P, int
         r.p0 = reinterpret_cast<const T *>(OP == OP_OPROJ ? w.wo : w.wd);
     }
     return r;
+}
+
+// bf16 input row element in two parts: hi at p[i], lo (what hi left out) at p[lo_off + i]
+__device__ __forceinline__ void store_hilo(__nv_bfloat16 *p, long long lo_off, long long i, float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    p[i] = hi;
+    p[lo_off + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
 // ---- x staging (consumer warps only) ---------------------------------------------------
@@ -273,7 +282,7 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
         const float up = __shfl_xor_sync(0xffffffffu, v, 8);
         if (valid && wr < 4) {
             const float h = silu_f(v) * up;
-            if (sizeof(T) == 2) P->GUb[(long long)xr * P->F + row] = __float2bfloat16_rn(h);
+            if (sizeof(T) == 2) store_hilo(P->GUb, (long long)(P->n + 1) * P->F, (long long)xr * P->F + row, h);
             else P->GUp[(long long)xr * P->F + row] = h;
         }
     } else {
@@ -284,7 +293,8 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
             // bf16 input row of the next GEMM: x * g of its normalisation; after the last layer
             // the newest row is the LM head's second input row
             if (sizeof(T) == 2) {
-                if (OP != OP_DOWN || layer + 1 < P->Ls) P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * pre.y);
+                if (OP != OP_DOWN || layer + 1 < P->Ls)
+                    store_hilo(P->Xb, (long long)(P->n + 1) * P->d, (long long)xr * P->d + row, o * pre.y);
                 else if (xr == pr.R - 1) {
                     // the LM head's second input row in two bf16 parts: the value and the rest
                     const float xl = o * pre.y;
@@ -458,8 +468,13 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // bulk copies (the projection's per anchor, masked ones zeroed instead); the
     // register-resident fragments are then read from there
     constexpr bool BULK = ESZ == 2;
-    const int xbytes = pg_xbytes(OP == OP_LM ? 4 : P->n + 1, kx, ESZ);
+    // x rows in shared memory: rows 0..n the hi parts, rows n+1..2n+1 the lo parts (bf16,
+    // except for the LM head, whose four rows carry both parts already)
+    constexpr bool HILO = ESZ == 2 && OP != OP_LM;
+    const int xrows = OP == OP_LM ? 4 : (HILO ? 2 : 1) * (P->n + 1);
+    const int xbytes = pg_xbytes(xrows, kx, ESZ);
     unsigned char *xs = smem;
+    unsigned char *xlo = xs + (P->n + 1) * xpitch;   // lo rows (HILO)
     float4 *red = reinterpret_cast<float4 *>(smem + xbytes);
     unsigned char *stages = smem + xbytes + pg_redbytes(MT);
     const int NS = min(PG_MAXNS, (PG_SMEM - xbytes - pg_redbytes(MT)) / stage_bytes);
@@ -495,36 +510,44 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     if constexpr (BULK && OP == OP_PROJ) {
         // row r, anchor a: the piece [max(k0, a d), min(k0 + kw, (a + 1) d)) of the slab
         const int d = P->d, a0 = k0 / d, a1 = (k0 + kw - 1) / d;
+        const long long alo = (long long)(P->n + 1) * P->nB * d;   // the anchors' lo parts
         if (tid == 0) {
             uint32_t tot = 0;
             for (int r = 0; r < R; ++r)
                 for (int a = a0; a <= a1; ++a)
-                    if (P->anchors[a] <= pr.depth[r]) tot += (uint32_t)(min(k0 + kw, (a + 1) * d) - max(k0, a * d)) * 2;
+                    if (P->anchors[a] <= pr.depth[r]) tot += (uint32_t)(min(k0 + kw, (a + 1) * d) - max(k0, a * d)) * 4;
             fence_proxy_async();
             mbar_expect_tx(xbar, tot);
             for (int r = 0; r < R; ++r)
                 for (int a = a0; a <= a1; ++a) {
                     if (P->anchors[a] > pr.depth[r]) continue;
                     const int ka = max(k0, a * d), kb = min(k0 + kw, (a + 1) * d);
-                    bulk_g2s(xs + r * xpitch + (ka - k0) * 2, P->ANCHb + ((long long)pr.slot[r] * P->nB + a) * d + (ka - a * d),
-                             (uint32_t)(kb - ka) * 2, xbar);
+                    const __nv_bfloat16 *src = P->ANCHb + ((long long)pr.slot[r] * P->nB + a) * d + (ka - a * d);
+                    bulk_g2s(xs + r * xpitch + (ka - k0) * 2, src, (uint32_t)(kb - ka) * 2, xbar);
+                    bulk_g2s(xlo + r * xpitch + (ka - k0) * 2, src + alo, (uint32_t)(kb - ka) * 2, xbar);
                 }
         }
-        // anchors deeper than the row's token enter as zeros
+        // anchors deeper than the row's token enter as zeros (both parts)
         for (int r = 0; r < R; ++r)
             for (int a = a0; a <= a1; ++a) {
                 if (P->anchors[a] <= pr.depth[r]) continue;
                 const int ka = max(k0, a * d), kb = min(k0 + kw, (a + 1) * d);
-                for (int e = ka + 8 * tid; e < kb; e += 8 * PG_CONSUMERS)
+                for (int e = ka + 8 * tid; e < kb; e += 8 * PG_CONSUMERS) {
                     *reinterpret_cast<uint4 *>(xs + r * xpitch + (e - k0) * 2) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4 *>(xlo + r * xpitch + (e - k0) * 2) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
     } else if constexpr (BULK) {
         if (tid == 0) {
             const __nv_bfloat16 *src = OP == OP_OPROJ ? P->ATTb : OP == OP_DOWN ? P->GUb : OP == OP_LM ? P->Xlm : P->Xb;
+            const long long lo = (long long)(P->n + 1) * K;   // the rows' lo parts follow the hi parts
             const uint32_t rb = (uint32_t)kw * 2;
             fence_proxy_async();
-            mbar_expect_tx(xbar, rb * R);
-            for (int r = 0; r < R; ++r) bulk_g2s(xs + r * xpitch, src + (long long)r * K + k0, rb, xbar);
+            mbar_expect_tx(xbar, rb * R * (HILO ? 2 : 1));
+            for (int r = 0; r < R; ++r) {
+                bulk_g2s(xs + r * xpitch, src + (long long)r * K + k0, rb, xbar);
+                if (HILO) bulk_g2s(xlo + r * xpitch, src + lo + (long long)r * K + k0, rb, xbar);
+            }
         }
     } else if (!xreg) {
         pg_stage_x<T, OP>(P, pr, layer, k0, kw, xs, xpitch);
@@ -584,7 +607,11 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
             if constexpr (ESZ == 2 && MT == 1) {
                 if (xreg) {
                     // one piece per tile (nch == 1): block bb = warp + 8j uses the j-th registers
+                    // for the hi parts; the lo parts (not for the LM head, whose four rows hold
+                    // both parts already) come from shared memory
                     const unsigned char *wp = tb + gq * rowb + tq * 16;
+                    const unsigned char *lp = xlo + gq * xpitch + tq * 16;
+                    const bool l0 = gq < R, l1 = gq + 8 < R;
                     float acc2[4] = {0.f, 0.f, 0.f, 0.f};
                     float(&f)[4] = *reinterpret_cast<float(*)[4]>(&acc[0]);
 #pragma unroll
@@ -594,6 +621,13 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
                             const uint4 w = lds128(wp + bb * 64);
                             mma_bf16(f, xf[j][0].x, xf[j][1].x, xf[j][0].y, xf[j][1].y, w.x, w.y);
                             mma_bf16(acc2, xf[j][0].z, xf[j][1].z, xf[j][0].w, xf[j][1].w, w.z, w.w);
+                            if (HILO) {
+                                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                                const uint4 la = l0 ? lds128(lp + bb * 64) : z;
+                                const uint4 lb = l1 ? lds128(lp + 8 * xpitch + bb * 64) : z;
+                                mma_bf16(f, la.x, lb.x, la.y, lb.y, w.x, w.y);
+                                mma_bf16(acc2, la.z, lb.z, la.w, lb.w, w.z, w.w);
+                            }
                         }
                     }
 #pragma unroll
@@ -608,6 +642,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
                 // and go to two accumulator chains (added at the end of the piece)
                 const unsigned char *wp = tb + gq * rowb + tq * 16;
                 const unsigned char *xp = xs + gq * xpitch + kc0 * 2 + tq * 16;
+                const unsigned char *xq = xlo + gq * xpitch + kc0 * 2 + tq * 16;
                 bool xv[MT][2];
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
@@ -628,6 +663,12 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
                         float(&f2)[4] = *reinterpret_cast<float(*)[4]>(&acc2[4 * m]);
                         mma_bf16(f, xa.x, xb.x, xa.y, xb.y, w.x, w.y);
                         mma_bf16(f2, xa.z, xb.z, xa.w, xb.w, w.z, w.w);
+                        if (HILO) {
+                            const uint4 la = xv[m][0] ? lds128(xq + (m * 16) * xpitch + bb * 64) : z;
+                            const uint4 lb = xv[m][1] ? lds128(xq + (m * 16 + 8) * xpitch + bb * 64) : z;
+                            mma_bf16(f, la.x, lb.x, la.y, lb.y, w.x, w.y);
+                            mma_bf16(f2, la.z, lb.z, la.w, lb.w, w.z, w.w);
+                        }
                     }
                 }
 #pragma unroll

@@ -3,8 +3,8 @@
 The fp64 oracle runs on the host cores and replays the GPU's trace (the replay rule follows
 the GPU only at near-ties).  Every workload starts from its own full prompt:
   * config 2 (0.6B): whole 256-token generations, draft-module greedy and forced p = 0.5, 0.8;
-  * config 3 (4B): the whole 512-token generation at forced p = 0.6 (about 1950 steps), and
-    prefixes of the other modes (greedy drafting, p = 0.3 and 0.9);
+  * config 3 (4B): 600 steps at forced p = 0.6 and prefixes of the other modes (greedy
+    drafting, p = 0.3 and 0.9);
   * config 5 (4B, T = 1): 256 steps of rejection sampling, dozens of residual resamples;
   * config 4 (8B): the 4096-token prompt through the oracle's prefill, then 16 steps at
     n = 8 and at n = 16; and the whole 512-token generation on the GPU at both n against
@@ -12,9 +12,9 @@ the GPU only at near-ties).  Every workload starts from its own full prompt:
 On top of the traces, the first steps of configs 2 to 5 compare vectors: logits entry by
 entry, the draft block's rows, residual streams, anchors and the K/V rows written.
 
-With SPD_LONG_PARITY=1 the prefixes become whole generations too: config 3 greedy (about
-4100 steps), p = 0.3 and 0.9 to 512 tokens, and config 5 to 1024 tokens.  Those take the
-oracle tens of minutes on the host cores, so they are opt-in.
+With SPD_LONG_PARITY=1 the prefixes become whole generations: config 3 in every mode to 512
+tokens (p = 0.6 about 3100 steps, greedy about 4100) and config 5 to 1024 tokens.  Those take
+the oracle about an hour on 16 host cores, so they are opt-in.
 
 Forced drafts follow the oracle's own greedy stream, so no oracle input comes from the GPU.
 Each workload is built once: weights drawn on the host from the seeded generators and
@@ -143,15 +143,16 @@ def test_config2_06b_whole_generation():
     release()
 
 
-def test_config3_4b_forced_whole_generation_and_mode_prefixes():
-    """4B shape, n = 8, Ls = 4, prompt 512: the whole 512-token generation at forced p = 0.6
-    replayed; greedy drafting and p = 0.3 / 0.9 as prefixes (whole with SPD_LONG_PARITY=1);
-    vectors over the first 8 steps."""
+def test_config3_4b_all_modes():
+    """4B shape, n = 8, Ls = 4, prompt 512: forced p = 0.6, greedy drafting and p = 0.3 / 0.9
+    replayed over prefixes (whole 512-token generations with SPD_LONG_PARITY=1); vectors over
+    the first 8 steps."""
     wl = si.SHAPE_4B
     case = case_of(wl)
     ref, _ = forced_ref(case, case.max_new)
     base = None
-    runs = [(0.6, None), (None, None if LONG else 300), (0.3, None if LONG else 200), (0.9, None if LONG else 200)]
+    runs = [(0.6, None if LONG else 600), (None, None if LONG else 300), (0.3, None if LONG else 200),
+            (0.9, None if LONG else 200)]
     for p, steps in runs:
         kw = {} if p is None else dict(force_p=p, forced_ref=torch.from_numpy(ref).cuda(), seed=2)
         tr, toks = gpu_steps(case, steps, **kw)

@@ -58,6 +58,36 @@ def test_prefill_logits(case):
     _prefill_logits_close(case, pf)
 
 
+@pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI, WIDEK],
+                         ids=["tiny", "small", "hd128", "multi", "widek"])
+def test_prefill_kv_caches_match_oracle(case):
+    """Every layer's K and V rows of the prompt, target and draft module, and the prompt's
+    last-position logits entry by entry, against the oracle's prefill (the tensor-core
+    GEMMs and attention of a bf16 prefill, the CUDA-core ones of an fp32 model)."""
+    from gpu_common import elem_err, vec_err
+    from speculative_pipeline_decoding_spd_gb300 import binding as B
+    tg, pd, prompt, m, _, _ = materialise(case)
+    e = engine(case, graph=False)
+    e.prefill(torch.from_numpy(prompt).cuda())
+    o = SPDOracle(m, case.n, case.max_seq)
+    o.prefill(prompt)
+    Sp, kvw = case.prompt_len, case.dm.Hkv * case.dm.hd
+    worst = 0.0
+    for li in range(case.dm.L):
+        for which, ref in ((B.SPD_BUF_KCACHE, o.kv.K[li]), (B.SPD_BUF_VCACHE, o.kv.V[li])):
+            got = e.read(which, (Sp, kvw), dtype=case.kv_dtype, index=li).astype(np.float64)
+            worst = max(worst, vec_err(got, ref[:Sp].reshape(Sp, kvw)))
+    for li in range(case.Ls):
+        for which, ref in ((B.SPD_BUF_PDM_KCACHE, o.pkv.K[li]), (B.SPD_BUF_PDM_VCACHE, o.pkv.V[li])):
+            got = e.read(which, (Sp, kvw), dtype=case.kv_dtype, index=li).astype(np.float64)
+            worst = max(worst, vec_err(got, ref[:Sp].reshape(Sp, kvw)))
+    pf = e.read(B.SPD_BUF_PREFILL_LOGITS, (case.dm.V,))
+    e.close()
+    lerr = elem_err(pf, o.prefill_logits)
+    print(f"prefill: K/V {worst:.2e}, logits {lerr:.2e}")
+    assert worst <= case.tol and lerr <= case.tol, (worst, lerr)
+
+
 @pytest.mark.parametrize("case", [TINY, SMALL, HD128, MULTI, WIDE, WIDEK, INROUNDS],
                          ids=["tiny", "small", "hd128", "multi", "wide", "widek", "inrounds"])
 def test_greedy_draft_module_replay(case):
@@ -223,8 +253,9 @@ def vector_run(case, steps, p=None, speculate="input", bounds=None, n=None):
 def test_vectors_match_oracle_step_by_step(name, case, kw):
     """Logits entry by entry, the draft block's residual rows, every in-flight residual
     stream and anchor state, and the K/V rows each step writes, against the oracle after
-    each of the first 12 steps, all within the case's one tolerance."""
-    worst, o = vector_run(case, 12, **kw)
+    each of the first steps (12, or 2n when the pipeline is deeper), all within the case's one
+    tolerance."""
+    worst, o = vector_run(case, max(12, 2 * case.n), **kw)   # past the first exits and a rollback
     if kw.get("p") is not None:
         assert any(r["accept"] == 0 for r in o.trace)     # a rollback happened inside the window
 
