@@ -10,7 +10,8 @@ the (untimed) prefill; value = committed tokens / device time.
 
 Modes: forced-<p> (drafts equal the greedy token with probability p), greedy (the draft
 module's argmax), t1 (the T = 1 workload: 4B shape, prompt 256, rejection sampling).
-Shapes: 4b (L36 d2560, prompt 512) and 8b (L36 d4096, prompt 4096, Ls 2).
+Shapes: tiny (fp32, L4 d256), 06b (L28 d1024, n 4), 4b (L36 d2560, prompt 512) and 8b (L36
+d4096, prompt 4096, Ls 2).
 
 Multi-GPU: independent replicas (one sequence per GPU, no collective on the data path);
 value = all ranks' committed tokens / max-over-ranks time.
@@ -48,7 +49,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--mode", default="forced-0.6", help="forced-<p>, greedy (draft-module argmax) or t1 (T = 1)")
-    ap.add_argument("--shape", default="4b", choices=["4b", "8b"])
+    ap.add_argument("--shape", default="4b", choices=["tiny", "06b", "4b", "8b"])
     ap.add_argument("--n", type=int, default=0, help="pipeline stages (default: the workload's)")
     ap.add_argument("--speculate", default="input", choices=["input", "output"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -84,7 +85,7 @@ def select_workload(args) -> si.Workload:
     if args.mode == "t1":
         wl = si.SHAPE_4B_T1
     else:
-        wl = si.SHAPE_8B if args.shape == "8b" else si.SHAPE_4B
+        wl = {"tiny": si.TINY, "06b": si.SHAPE_06B, "4b": si.SHAPE_4B, "8b": si.SHAPE_8B}[args.shape]
     if args.n:
         wl = si.Workload(wl.name, wl.dims, n=args.n, anchors=wl.anchors, Ls=wl.Ls, prompt_len=wl.prompt_len,
                          max_new=wl.max_new, temperature=wl.temperature, forced_p=wl.forced_p)
@@ -179,7 +180,7 @@ def gateup_bytes(trace, dm, n):
     the occupied stages that hold a j-th layer stream 2 x F x d bf16 weights."""
     sizes = stage_sizes(dm.L, n)
     J = max(sizes)
-    per = 2 * dm.F * dm.d * 2
+    per = 2 * dm.F * dm.d * (2 if dm.dtype == "bf16" else 4)
     tot, launches = 0, 0
     for r in trace:
         m = r["n_active"]
@@ -217,7 +218,14 @@ def run_gb300(args, ws, rank, local):
     # programmatic launch overlap of the kernels around them)
     e = Engine(dm, tg, pd, n, WL.anchors, max_seq=max_seq, max_new=max_new, seed=2,
                force_p=(-1.0 if p is None else p), forced_ref=forced_ref, graph=True, timing=False, **spec)
+    # the prefill is not part of the metric; its time is reported beside it (second of two runs)
     e.prefill(prompt)
+    pf0, pf1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pf0.record()
+    e.prefill(prompt)
+    pf1.record()
+    torch.cuda.synchronize()
+    prefill_ms = pf0.elapsed_time(pf1)
     e.step(args.warmup)
     N0 = e.stats()["N"]
     K0 = e.stats()["K"]
@@ -245,7 +253,7 @@ def run_gb300(args, ws, rank, local):
     commits = N1 - N0
     # weight bytes streamed by the timed steps (occupied stages + draft module + LM head)
     sizes = stage_sizes(dm.L, n)
-    el = 2
+    el = 2 if dm.dtype == "bf16" else 4
     layer_b = el * ((dm.Hq + 2 * dm.Hkv) * dm.hd * dm.d + dm.d * dm.Hq * dm.hd + 3 * dm.F * dm.d)
     pdm_b = el * (dm.d * len(WL.anchors) * dm.d) + WL.Ls * layer_b
     lm_b = el * dm.V * dm.d
@@ -279,6 +287,7 @@ def run_gb300(args, ws, rank, local):
     if args.skip_e2e:
         return dict(ms=ms, commits=commits, steps=args.steps, wbytes=wbytes, gate_bytes=gb, gate_ms=g_ms,
                     gate_launches=gl, clocks=clocks, alpha=commits / args.steps, e2e_tokens=0, e2e_s=float("nan"),
+                    prefill_ms=prefill_ms,
                     e2e_steps=1, max_new=max_new, prompt_len=WL.prompt_len,
                     launches_per_step=5 * max(sizes) + 1 + 5 * WL.Ls + 2)
     e2 = Engine(dm, tg, pd, n, WL.anchors, max_seq=WL.prompt_len + WL.max_new + n + 8, max_new=WL.max_new, seed=2,
@@ -293,7 +302,8 @@ def run_gb300(args, ws, rank, local):
     e2.close()
     return dict(ms=ms, commits=commits, steps=args.steps, wbytes=wbytes, gate_bytes=gb, gate_ms=g_ms, gate_launches=gl,
                 clocks=clocks, alpha=commits / args.steps, e2e_tokens=len(toks), e2e_s=e2_s, e2e_steps=e2_steps,
-                max_new=max_new, prompt_len=WL.prompt_len, launches_per_step=5 * max(sizes) + 1 + 5 * WL.Ls + 2)
+                prefill_ms=prefill_ms, max_new=max_new, prompt_len=WL.prompt_len,
+                launches_per_step=5 * max(sizes) + 1 + 5 * WL.Ls + 2)
 
 
 # ---------------------------------------------------------------------------------------
@@ -364,6 +374,8 @@ def main():
         if tj.get("k_target_sha") == source_hash(src) and tj.get("d") == WL.dims.d and tj.get("F") == WL.dims.F:
             per_stage_layer = tj["dram_bytes_per_stage_layer"]
             traffic = per_stage_layer * (r["gate_bytes"] / (2 * WL.dims.F * WL.dims.d * 2)) / r["gate_launches"]
+        else:
+            traffic = None
     ms_step = ms_max / args.steps
     a_cf = alpha_ref(args.mode, WL.n) if p is not None else None
     wgbs = r["wbytes"] / (r["ms"] / 1e3) / 1e9
@@ -378,7 +390,7 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if WL.dims.dtype == "bf16" else "f32",
         "data": "synthetic (seeded random-init weights drawn on the GPU, uniform-random prompt ids)",
         "config": {"workload": f"{WL.name}: L{WL.dims.L} d{WL.dims.d} {WL.dims.Hq}q/{WL.dims.Hkv}kv x{WL.dims.hd} "
                                f"F{WL.dims.F} V{WL.dims.V}, n={WL.n}, Ls={WL.Ls}, "
@@ -390,6 +402,7 @@ def main():
                    "alpha": round(r["alpha"], 4), "S0": round(r["alpha"] * WL.n, 3),
                    "tok_s_at_closed_form_alpha": None if a_cf is None else round(a_cf * 1e3 / ms_step, 2),
                    "closed_form_alpha": None if a_cf is None else round(a_cf, 4),
+                   "prefill_ms": round(r["prefill_ms"], 3),
                    "weight_GBps": round(wgbs, 1),
                    "weight_frac_of_measured_hbm": round(wgbs / hbm, 4),
                    "weight_frac_of_nominal_hbm": round(wgbs / NOMINAL_HBM_GBS, 4),
@@ -438,13 +451,16 @@ def main_reference(args, ws, rank):
     """The oracle (plain fp64 CPU restatement of the method) on this arm's workload.  Each
     timed step is one pipeline step of the oracle; value = steps/s x the same alpha the
     GPU arm's cpu_baseline uses (closed form where one exists, else the oracle sample's
-    own commit rate).  e2e: the workload's own prompt, prefill and steps timed together."""
+    own commit rate after the pipeline fill).  e2e: the workload's own prompt, prefill and steps timed together."""
     if rank != 0:
         return
     k = max(1, min(args.steps, 12))
     w = max(0, min(args.warmup, 2))
+    if alpha_ref(args.mode, WL.n) is None:
+        k = max(k, 2 * WL.n - w)   # no closed form: the sample must reach past the pipeline fill
     sps, commits, dt, _, cores = oracle_sample(k + w, args.mode)
-    alpha = cpu_alpha(args.mode, WL.n, commits / (k + w))
+    # commits per step after the first n - 1 steps (no token leaves before them)
+    alpha = cpu_alpha(args.mode, WL.n, commits / max(1, k + w - (WL.n - 1)))
     value = sps * alpha
     e_sps, e_commits, e_dt, e_pf, _ = oracle_sample(4, args.mode, e2e=True)
     e2e_tokens = 1 + 4 * alpha

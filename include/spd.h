@@ -178,7 +178,9 @@ typedef struct spd_trace_rec {
 
 typedef struct spd_handle spd_handle;
 
-/* Bytes of device workspace spd_create needs for these shapes (no device work). */
+/* Bytes of device workspace spd_create needs for these shapes (no device work).  Of
+ * pdm_shape_only only the Ls field is read (the draft module's shape; its pointers may be
+ * NULL); NULL means no draft module. */
 int spd_workspace_bytes(const spd_dims *d, const spd_pdm_weights *pdm_shape_only, const spd_config *cfg,
                         size_t *bytes);
 
@@ -232,6 +234,18 @@ int spd_generate(spd_handle *h, const int32_t *prompt, int32_t prompt_len, int32
  * Synchronises.  SPD_ECUDA on a failed copy. */
 int spd_get_trace(spd_handle *h, spd_trace_rec *recs_host, int32_t max_recs, int32_t *len_host,
                   int32_t *count_host);
+
+/* Device view of the trace: records [count] and per-layer KV valid lengths [count][L],
+ * both in the handle's workspace (valid until the next spd_prefill / spd_generate /
+ * spd_reset / spd_destroy; read them on or after the handle's stream).  Synchronises to read
+ * the count.  The same records as spd_get_trace without a copy. */
+typedef struct spd_trace_view {
+    const spd_trace_rec *recs;
+    const int32_t *kv_len;
+    int32_t count;
+    int32_t L;
+} spd_trace_view;
+int spd_get_trace_view(spd_handle *h, spd_trace_view *out);
 
 /* Statistics so far (synchronises). */
 int spd_get_stats(spd_handle *h, spd_stats *stats_host);

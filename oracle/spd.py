@@ -87,19 +87,30 @@ class Replay:
     mismatches: list = dataclasses.field(default_factory=list)
     adopted: int = 0
     decisions: int = 0
+    # the same two counts per kind of decision: "argmax", "sample", "keep"
+    adopted_by: dict = dataclasses.field(default_factory=lambda: {"argmax": 0, "sample": 0, "keep": 0})
+    decisions_by: dict = dataclasses.field(default_factory=lambda: {"argmax": 0, "sample": 0, "keep": 0})
+
+    def _count(self, kind: str, adopted: bool):
+        self.decisions += 1
+        self.decisions_by[kind] += 1
+        if adopted:
+            self.adopted += 1
+            self.adopted_by[kind] += 1
 
     def pick_argmax(self, z: np.ndarray, other: Optional[int], what: str, t: int) -> int:
         mine = argmax_fp32(z)
         if other is None:
             return mine
-        self.decisions += 1
         if other == mine:
+            self._count("argmax", False)
             return mine
         z32 = z.astype(np.float64)
         top = z32[mine]
         if z32[other] >= top - self.tol * abs(top):
-            self.adopted += 1
+            self._count("argmax", True)
             return int(other)
+        self._count("argmax", False)
         self.mismatches.append((t, what, mine, int(other), float(top - z32[other])))
         return mine
 
@@ -107,8 +118,8 @@ class Replay:
         mine = inverse_cdf(w, u)
         if other is None:
             return mine
-        self.decisions += 1
         if other == mine:
+            self._count("sample", False)
             return mine
         c = np.cumsum(w) / np.sum(w)
         # the other pick owns the interval [c[other-1], c[other]) of the unit line; it is
@@ -117,8 +128,9 @@ class Replay:
         if 0 <= other < len(w) and w[other] > 0.0:
             lo = c[other - 1] if other > 0 else 0.0
             if lo - self.tol_u <= u < c[other] + self.tol_u:
-                self.adopted += 1
+                self._count("sample", True)
                 return int(other)
+        self._count("sample", False)
         self.mismatches.append((t, what, mine, int(other), float(u)))
         return mine
 
@@ -126,12 +138,13 @@ class Replay:
         mine = bool(u1 < ratio)
         if other is None:
             return mine
-        self.decisions += 1
         if bool(other) == mine:
+            self._count("keep", False)
             return mine
         if abs(u1 - ratio) <= self.tol * max(ratio, 1e-30) or abs(u1 - ratio) <= self.tol_u:
-            self.adopted += 1
+            self._count("keep", True)
             return bool(other)
+        self._count("keep", False)
         self.mismatches.append((t, "keep", int(mine), int(other), float(u1 - ratio)))
         return mine
 

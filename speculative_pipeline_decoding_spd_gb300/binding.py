@@ -66,6 +66,10 @@ class spd_trace_rec(C.Structure):
                 ("pdm_logit", C.c_float)]
 
 
+class spd_trace_view(C.Structure):
+    _fields_ = [("recs", C.c_void_p), ("kv_len", C.c_void_p), ("count", C.c_int32), ("L", C.c_int32)]
+
+
 _lib = None
 
 # (name, restype, argtypes) of every entry point declared in include/spd.h
@@ -79,6 +83,7 @@ SIGNATURES = [
     ("spd_generate", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.POINTER(C.c_int32),
                                C.POINTER(spd_stats)]),
     ("spd_get_trace", C.c_int, [C.c_void_p, C.POINTER(spd_trace_rec), C.c_int32, C.c_void_p, C.POINTER(C.c_int32)]),
+    ("spd_get_trace_view", C.c_int, [C.c_void_p, C.POINTER(spd_trace_view)]),
     ("spd_get_stats", C.c_int, [C.c_void_p, C.POINTER(spd_stats)]),
     ("spd_get_tokens", C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.POINTER(C.c_int32)]),
     ("spd_read_buffer", C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_size_t, C.c_void_p, C.c_size_t]),
@@ -162,6 +167,12 @@ def spd_get_trace(h, max_recs: int, len_ptr: int = 0):
     cnt = C.c_int32(0)
     check(load().spd_get_trace(h, recs, max_recs, C.c_void_p(len_ptr) if len_ptr else None, C.byref(cnt)), h)
     return recs, cnt.value
+
+
+def spd_get_trace_view(h) -> spd_trace_view:
+    v = spd_trace_view()
+    check(load().spd_get_trace_view(h, C.byref(v)), h)
+    return v
 
 
 def spd_get_stats(h):

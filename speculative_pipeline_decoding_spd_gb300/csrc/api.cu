@@ -146,10 +146,10 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.QKVp = b.take<float>((size_t)ns * qkv);
     h.ATTp = b.take<float>((size_t)ns * qr);
     h.GUp = b.take<float>((size_t)ns * d->F);
-    // bf16 input rows of the draft GEMMs: hi parts, then lo parts of the same size
-    h.Xb = b.take<__nv_bfloat16>((size_t)2 * ns * d->d);
-    h.ATTb = b.take<__nv_bfloat16>((size_t)2 * ns * qr);
-    h.GUb = b.take<__nv_bfloat16>((size_t)2 * ns * d->F);
+    // bf16 input rows of the draft GEMMs (the anchors: hi parts, then lo parts)
+    h.Xb = b.take<__nv_bfloat16>((size_t)ns * d->d);
+    h.ATTb = b.take<__nv_bfloat16>((size_t)ns * qr);
+    h.GUb = b.take<__nv_bfloat16>((size_t)ns * d->F);
     h.Xlm = b.take<__nv_bfloat16>((size_t)4 * d->d);
     h.ANCHb = b.take<__nv_bfloat16>((size_t)2 * ns * c->n_anchors * d->d);
     h.ssp = b.take<float>((size_t)MAXS * (d->d / 8));
@@ -167,6 +167,7 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.logits = b.take<float>((size_t)2 * d->V);
     h.dlogits = b.take<float>(c->temperature > 0.f ? (size_t)ns * d->V : 1);
     h.lm_part = b.take<float>((size_t)LM_GRID_MAX * 4);
+    h.lm_stat = b.take<float>((size_t)LM_GRID_MAX * 4);
     h.lm_cnt = b.take<int>(1);
     h.trace = b.take<spd_trace_rec>((size_t)max_steps);
     h.trace_len = b.take<int>((size_t)max_steps * d->L);
@@ -397,6 +398,7 @@ extern "C" int spd_create(const spd_dims *d, const spd_target_weights *tw, const
     H->num_sms = std::min(H->num_sms, SM_BOUND);
     H->grid_gemv = H->num_sms * target_blocks_per_sm(h.dtype, gemv_smem_bytes(h));
     H->grid_lm = std::min(LM_GRID_MAX, H->num_sms * lm_blocks_per_sm(h.dtype, 2 * h.d * 4, h.pdm_lm_head == h.lm_head));
+    h.lm_stats = (lm_on_tensor_cores(h) && h.temperature > 0.f) ? 1 : 0;
     if (cudaStreamCreateWithFlags(&H->s_main, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&H->s_pdm, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&H->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
@@ -635,6 +637,17 @@ extern "C" int spd_get_trace(spd_handle *H, spd_trace_rec *recs, int32_t max_rec
     if (recs && k) CK(H, cudaMemcpy(recs, H->h.trace, (size_t)k * sizeof(spd_trace_rec), cudaMemcpyDeviceToHost));
     if (len_host && k) CK(H, cudaMemcpy(len_host, H->h.trace_len, (size_t)k * H->h.L * sizeof(int), cudaMemcpyDeviceToHost));
     if (count_host) *count_host = t;
+    return SPD_OK;
+}
+
+extern "C" int spd_get_trace_view(spd_handle *H, spd_trace_view *out) {
+    if (!H || !out) return SPD_EINVAL;
+    CK(H, cudaMemcpyAsync(H->host_pinned, &H->h.st->t, sizeof(int), cudaMemcpyDeviceToHost, H->s_main));
+    CK(H, cudaStreamSynchronize(H->s_main));
+    out->recs = H->h.trace;
+    out->kv_len = H->h.trace_len;
+    out->count = std::min(H->host_pinned[0], H->h.max_steps);
+    out->L = H->h.L;
     return SPD_OK;
 }
 

@@ -22,47 +22,101 @@ constexpr int VT = 256;   // verify kernel threads
 __device__ __forceinline__ float u01(uint32_t w) { return (float)(w >> 8) * (1.0f / 16777216.0f); }
 
 // Block-wide inverse-CDF draw over weights w(i), i in [0, V): the smallest i whose running
-// sum (index order) exceeds u * total.  Threads own contiguous index ranges; the range
-// totals are scanned in thread order, the crossing range is scanned sequentially.
+// sum (index order) exceeds u * total.  The ids are cut into tiles of 512 (16 per lane of a
+// warp): pass 1, each warp sums its tiles (tiles w, w + 8, ...; lane l reads ids l, l + 32,
+// ..., coalesced) with no block-wide barrier inside the loop; warp 0 then runs the running
+// sum over the tile totals in tile order (32 tiles per warp-wide scan), and scans the
+// crossing tile again with lane l owning the contiguous slice [16 l, 16 l + 16).
 // Returns the index in all threads; *total_out receives the total.
+constexpr int SAMPLE_PER = 16;
+constexpr int SAMPLE_TILE = 32 * SAMPLE_PER;
+constexpr int SAMPLE_MAX_TILES = 512;   // V up to 262144
+
+__device__ __forceinline__ float warp_incl_scan(float v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    return v;
+}
+
 template <typename WF>
 __device__ int block_sample(int V, float u, WF wf, float *red, float *total_out) {
-    __shared__ float s_part[VT];
+    __shared__ float s_tile[SAMPLE_MAX_TILES];
     __shared__ int s_pick;
-    const int per = (V + VT - 1) / VT;
-    const int lo = threadIdx.x * per, hi = min(V, lo + per);
-    float loc = 0.f;
-    for (int i = lo; i < hi; ++i) loc += wf(i);
-    s_part[threadIdx.x] = loc;
-    if (threadIdx.x == 0) s_pick = -1;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float tot = 0.f;
-        for (int t = 0; t < VT; ++t) tot += s_part[t];
-        red[0] = tot;
-        const float target = u * tot;
-        float acc = 0.f;
-        int th = VT - 1;
-        for (int t = 0; t < VT; ++t) {
-            if (acc + s_part[t] > target && s_part[t] > 0.f) { th = t; break; }
-            acc += s_part[t];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int ntiles = (V + SAMPLE_TILE - 1) / SAMPLE_TILE;
+    for (int t = warp; t < ntiles; t += nw) {
+        const int base = t * SAMPLE_TILE;
+        float v[SAMPLE_PER];
+#pragma unroll
+        for (int j = 0; j < SAMPLE_PER; ++j) {
+            const int i = base + j * 32 + lane;
+            v[j] = i < V ? wf(i) : 0.f;
         }
-        red[1] = acc;
-        red[2] = __int_as_float(th);
+        float loc = 0.f;
+#pragma unroll
+        for (int j = 0; j < SAMPLE_PER; ++j) loc += v[j];
+        loc = warp_sum(loc);
+        if (lane == 0) s_tile[t] = loc;
     }
     __syncthreads();
-    const int th = __float_as_int(red[2]);
-    if ((int)threadIdx.x == th) {
-        float acc = red[1];
-        const float target = u * red[0];
-        int pick = -1, lastnz = -1;
-        for (int i = lo; i < hi; ++i) {
-            const float w = wf(i);
-            if (w > 0.f) lastnz = i;
-            acc += w;
-            if (acc > target && w > 0.f) { pick = i; break; }
+    if (warp == 0) {
+        float tot = 0.f;
+        for (int t = lane; t < ntiles; t += 32) tot += s_tile[t];
+        tot = warp_sum(tot);
+        const float target = u * tot;
+        // the crossing tile
+        float before = 0.f;
+        int ct = -1;
+        for (int t0 = 0; t0 < ntiles; t0 += 32) {
+            const int t = t0 + lane;
+            const float w = t < ntiles ? s_tile[t] : 0.f;
+            const float inc = warp_incl_scan(w);
+            const unsigned hit = __ballot_sync(0xffffffffu, t < ntiles && w > 0.f && before + inc > target);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                before += __shfl_sync(0xffffffffu, inc - w, l);
+                ct = t0 + l;
+                break;
+            }
+            before += __shfl_sync(0xffffffffu, inc, 31);
         }
-        s_pick = pick >= 0 ? pick : (lastnz >= 0 ? lastnz : lo);
+        int pick = -1, lastnz = -1;
+        if (ct < 0) {
+            // rounding left the target beyond the running sum: the last id with weight
+            ct = ntiles - 1;
+            for (int t = ntiles - 1; t >= 0; --t)
+                if (s_tile[t] > 0.f) { ct = t; break; }
+            before = -INFINITY;   // every weighted id below crosses; the scan below keeps the last
+        }
+        // the crossing tile, lane l owning ids [16 l, 16 l + 16) of it
+        const int lo = ct * SAMPLE_TILE + lane * SAMPLE_PER;
+        float w[SAMPLE_PER], sl = 0.f;
+#pragma unroll
+        for (int j = 0; j < SAMPLE_PER; ++j) {
+            w[j] = lo + j < V ? wf(lo + j) : 0.f;
+            sl += w[j];
+        }
+        const float inc = warp_incl_scan(sl);
+        const unsigned hit = __ballot_sync(0xffffffffu, sl > 0.f && before + inc > target);
+        const unsigned nz = __ballot_sync(0xffffffffu, sl > 0.f);
+        const int hl = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : 0);
+        if (lane == hl) {
+            float acc = before == -INFINITY ? 0.f : before + inc - sl;
+            for (int j = 0; j < SAMPLE_PER; ++j) {
+                if (w[j] > 0.f) lastnz = lo + j;
+                acc += w[j];
+                if (hit && acc > target && w[j] > 0.f) {
+                    pick = lo + j;
+                    break;
+                }
+            }
+            s_pick = pick >= 0 ? pick : (lastnz >= 0 ? lastnz : min(lo, V - 1));
+            red[0] = tot;
+        }
     }
     __syncthreads();
     if (total_out) *total_out = red[0];
@@ -71,16 +125,31 @@ __device__ int block_sample(int V, float u, WF wf, float *red, float *total_out)
     return pick;
 }
 
-// max and sum of exp(z/T - max) over a logits row (fixed reduction order)
+// max and sum of exp(z/T - max) over a logits row in one coalesced pass: each thread keeps a
+// running max and a sum rescaled when its max grows, then the threads' pairs are merged by a
+// fixed tree
 __device__ void softmax_stats(const float *z, int V, float invT, float *red, float *m_out, float *s_out) {
-    float m = -INFINITY;
-    for (int i = threadIdx.x; i < V; i += blockDim.x) m = fmaxf(m, z[i] * invT);
-    m = block_max(m, red);
-    float s = 0.f;
-    for (int i = threadIdx.x; i < V; i += blockDim.x) s += expf(z[i] * invT - m);
-    s = block_sum(s, red);
-    *m_out = m;
-    *s_out = s;
+    float m = -INFINITY, sum = 0.f;
+    for (int i0 = threadIdx.x; i0 < V; i0 += 4 * blockDim.x) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * blockDim.x;
+            v[j] = i < V ? z[i] * invT : -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (v[j] > m) {
+                sum = sum * expf(m - v[j]);
+                m = v[j];
+            }
+            if (v[j] > -INFINITY) sum += expf(v[j] - m);
+        }
+    }
+    const float M = block_max(m, red);
+    const float S = block_sum(m == -INFINITY ? 0.f : sum * expf(m - M), red);
+    *m_out = M;
+    *s_out = S;
 }
 
 template <typename T>
@@ -182,17 +251,26 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
     }
     __syncthreads();
     if (!P->forced && T_ > 0.f) {
-        // sample the draft from softmax(z_D / T) and keep its normalisers with the slot
-        const float *zd = P->dlogits + (long long)s_newslot * V;
-        const float invT = 1.0f / T_;
-        float m, s;
-        softmax_stats(zd, V, invT, red, &m, &s);
-        const float u0 = u01(philox_word0((uint32_t)t, 0u, P->seed_lo, P->seed_hi));
-        const int pick = block_sample(V, u0, [&](int i) { return expf(zd[i] * invT - m); }, red + 4, nullptr);
-        if (threadIdx.x == 0) {
-            s_draft = pick;
-            st->dmax[s_newslot] = m;
-            st->dsum[s_newslot] = s;
+        // sample the draft from softmax(z_D / T) and keep its normalisers with the slot (the
+        // tensor-core LM head has drawn it already, from the same uniform)
+        if (P->lm_stats) {
+            if (threadIdx.x == 0) {
+                s_draft = st->samp;
+                st->dmax[s_newslot] = st->lmM[1];
+                st->dsum[s_newslot] = st->lmS[1];
+            }
+        } else {
+            const float *zd = P->dlogits + (long long)s_newslot * V;
+            const float invT = 1.0f / T_;
+            float m, s;
+            softmax_stats(zd, V, invT, red, &m, &s);
+            const float u0 = u01(philox_word0((uint32_t)t, 0u, P->seed_lo, P->seed_hi));
+            const int pick = block_sample(V, u0, [&](int i) { return expf(zd[i] * invT - m); }, red + 4, nullptr);
+            if (threadIdx.x == 0) {
+                s_draft = pick;
+                st->dmax[s_newslot] = m;
+                st->dsum[s_newslot] = s;
+            }
         }
         __syncthreads();
     }
@@ -211,7 +289,12 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
             const float *zt = P->logits;
             const float *zd = P->dlogits + (long long)s_xslot * V;
             float tm, ts;
-            softmax_stats(zt, V, invT, red, &tm, &ts);
+            if (P->lm_stats) {
+                tm = st->lmM[0];
+                ts = st->lmS[0];
+            } else {
+                softmax_stats(zt, V, invT, red, &tm, &ts);
+            }
             if (threadIdx.x == 0) {
                 const int x = s_x;
                 const float pt = expf(zt[x] * invT - tm) / ts;

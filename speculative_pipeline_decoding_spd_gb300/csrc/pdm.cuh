@@ -8,10 +8,13 @@
 // tokens, at consecutive positions.
 //
 // Every GEMM here multiplies one weight matrix W [N][K] by R <= n+1 row vectors x [R][K]
-// (far more bytes of W than of x: bound by streaming W once from HBM).  With bf16 weights
-// each x row arrives as two bf16 rows, hi = bf16(x) and lo = bf16(x - hi), and both meet the
-// weights on the tensor cores (the products add up in the same accumulators), so the
-// GEMM sees x at about 16 mantissa bits, not 8.  A group of CTAs does one GEMM; per CTA:
+// (far more bytes of W than of x: bound by streaming W once from HBM).  With bf16 weights the
+// projection's input (the concatenated anchors) arrives as two bf16 rows per row, hi = bf16(x)
+// and lo = bf16(x - hi), and both meet the weights on the tensor cores (the products add up
+// in the same accumulators), so the projection sees its input at about 16 mantissa bits.  Its
+// rounding dominates the module's: in fp64 on the 4B shape, rounding only the projection's
+// input to bf16 moves the draft logits by 7.5e-3 of their scale, any one of the layers'
+// GEMM inputs by 0.3e-3 to 2.1e-3.  A group of CTAs does one GEMM; per CTA:
 //   * a producer warp streams 8-row tiles of W (each row piece up to 6 KB, 1-D bulk
 //     copies) into a shared-memory ring signalled by mbarriers;
 //   * the R rows of x for the CTA's K slab go to shared memory: for bf16 weights the kernel
@@ -137,12 +140,8 @@ __device__ __forceinline__ PgRows<T, OP> pg_rows(const Plan *__restrict__ P, int
     return r;
 }
 
-// bf16 input row element in two parts: hi at p[i], lo (what hi left out) at p[lo_off + i]
-__device__ __forceinline__ void store_hilo(__nv_bfloat16 *p, long long lo_off, long long i, float v) {
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    p[i] = hi;
-    p[lo_off + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
-}
+// Draft GEMMs whose bf16 input rows come as hi and lo parts (the projection's anchors).
+template <int OP> __host__ __device__ constexpr bool pg_hilo() { return OP == OP_PROJ; }
 
 // ---- x staging (consumer warps only) ---------------------------------------------------
 template <typename XT>
@@ -282,7 +281,7 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
         const float up = __shfl_xor_sync(0xffffffffu, v, 8);
         if (valid && wr < 4) {
             const float h = silu_f(v) * up;
-            if (sizeof(T) == 2) store_hilo(P->GUb, (long long)(P->n + 1) * P->F, (long long)xr * P->F + row, h);
+            if (sizeof(T) == 2) P->GUb[(long long)xr * P->F + row] = __float2bfloat16_rn(h);
             else P->GUp[(long long)xr * P->F + row] = h;
         }
     } else {
@@ -293,8 +292,7 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
             // bf16 input row of the next GEMM: x * g of its normalisation; after the last layer
             // the newest row is the LM head's second input row
             if (sizeof(T) == 2) {
-                if (OP != OP_DOWN || layer + 1 < P->Ls)
-                    store_hilo(P->Xb, (long long)(P->n + 1) * P->d, (long long)xr * P->d + row, o * pre.y);
+                if (OP != OP_DOWN || layer + 1 < P->Ls) P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * pre.y);
                 else if (xr == pr.R - 1) {
                     // the LM head's second input row in two bf16 parts: the value and the rest
                     const float xl = o * pre.y;
@@ -383,14 +381,24 @@ static __device__ __noinline__ void pg_lm_inv_rms(const Plan *__restrict__ P, co
 // Argmax of the two logit rows (lowest id on ties): the CTA's candidates (held by the
 // reduction threads of x rows 0 and 1, one per tile slot) are reduced in slot order, then
 // the last CTA to finish merges the CTAs' results and leaves top / topval in the state.
-static __device__ __noinline__ void pg_lm_argmax(const Plan *__restrict__ P, int xr, int wr, float bv, int bi) {
-    __shared__ float s_lv[2][PG_RG];
+// At T > 0 the same threads also carry their outputs' softmax statistics (running max of
+// z/T and the sum of exp(z/T - max)): the CTA merges them in slot order, the last CTA merges
+// the CTAs' in CTA order into the rows' normalisers, and draws the draft token from row 1 by
+// inverse CDF (the smallest id whose running sum in id order exceeds u * total; CTAs hold
+// consecutive id ranges, so the running sum is the CTA totals' prefix, then the crossing
+// CTA's ids one warp-wide scan at a time).
+static __device__ __noinline__ void pg_lm_argmax(const Plan *__restrict__ P, int xr, int wr, float bv, int bi, float sm,
+                                                 float ss, int G8) {
+    __shared__ float s_lv[2][PG_RG], s_sm[2][PG_RG], s_ss[2][PG_RG];
     __shared__ int s_li[2][PG_RG];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool stats = P->lm_stats != 0;
     if (tid < 128 && xr < 2) {
         s_lv[xr][wr] = bv;
         s_li[xr][wr] = bi;
+        s_sm[xr][wr] = sm;
+        s_ss[xr][wr] = ss;
     }
     named_sync(PG_BAR, PG_CONSUMERS);
     if (tid < 2) {
@@ -403,6 +411,15 @@ static __device__ __noinline__ void pg_lm_argmax(const Plan *__restrict__ P, int
             }
         P->lm_part[blockIdx.x * 4 + tid * 2] = cv;
         P->lm_part[blockIdx.x * 4 + tid * 2 + 1] = __int_as_float(ci);
+        if (stats) {
+            float m = -INFINITY;
+            for (int w = 0; w < PG_RG; ++w) m = fmaxf(m, s_sm[tid][w]);
+            float sum = 0.f;
+            for (int w = 0; w < PG_RG; ++w)
+                if (s_sm[tid][w] > -INFINITY) sum += s_ss[tid][w] * expf(s_sm[tid][w] - m);
+            P->lm_stat[blockIdx.x * 4 + tid * 2] = m;
+            P->lm_stat[blockIdx.x * 4 + tid * 2 + 1] = sum;
+        }
     }
     __threadfence();
     named_sync(PG_BAR, PG_CONSUMERS);
@@ -410,11 +427,12 @@ static __device__ __noinline__ void pg_lm_argmax(const Plan *__restrict__ P, int
     named_sync(PG_BAR, PG_CONSUMERS);
     if (!s_last) return;
     __threadfence();
+    const int nc = (int)gridDim.x;
     if (warp < 2) {
         const int row = warp;
         float cv = -INFINITY;
         int ci = 0x7fffffff;
-        for (int c = lane; c < (int)gridDim.x; c += 32) {
+        for (int c = lane; c < nc; c += 32) {
             const float v = __ldcg(P->lm_part + c * 4 + row * 2);
             const int id = __float_as_int(__ldcg(P->lm_part + c * 4 + row * 2 + 1));
             if (v > cv || (v == cv && id < ci)) {
@@ -434,6 +452,75 @@ static __device__ __noinline__ void pg_lm_argmax(const Plan *__restrict__ P, int
         if (lane == 0) {
             P->st->top[row] = ci;
             P->st->topval[row] = cv;
+        }
+        if (stats) {
+            // the row's normaliser: max over the CTAs, then sum_c s_c e^{m_c - M} (lane-strided in
+            // CTA order, then a fixed shuffle tree)
+            float M = -INFINITY;
+            for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(P->lm_stat + c * 4 + row * 2));
+            M = warp_max(M);
+            float S = 0.f;
+            for (int c = lane; c < nc; c += 32) {
+                const float mc = __ldcg(P->lm_stat + c * 4 + row * 2);
+                if (mc > -INFINITY) S += __ldcg(P->lm_stat + c * 4 + row * 2 + 1) * expf(mc - M);
+            }
+            S = warp_sum(S);
+            if (lane == 0) {
+                P->st->lmM[row] = M;
+                P->st->lmS[row] = S;
+            }
+            if (row == 1 && !P->forced) {
+                // the draft token: u0 = the step's purpose-0 uniform
+                const uint32_t t = (uint32_t)(P->st->t + 1);
+                const float u0 = (float)(philox_word0(t, 0u, P->seed_lo, P->seed_hi) >> 8) * (1.0f / 16777216.0f);
+                const float target = u0 * S;
+                // the crossing CTA: running sum of the CTA totals in CTA order, 32 at a time
+                float before = 0.f;
+                int cstar = nc - 1;
+                for (int c0 = 0; c0 < nc; c0 += 32) {
+                    const int c = c0 + lane;
+                    const float mc = c < nc ? __ldcg(P->lm_stat + c * 4 + 2) : -INFINITY;
+                    const float w = mc > -INFINITY ? __ldcg(P->lm_stat + c * 4 + 3) * expf(mc - M) : 0.f;
+                    float inc = w;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, inc, o);
+                        if (lane >= o) inc += y;
+                    }
+                    const unsigned hit = __ballot_sync(0xffffffffu, c < nc && w > 0.f && before + inc > target);
+                    if (hit) {
+                        const int l = __ffs(hit) - 1;
+                        const float ex = __shfl_sync(0xffffffffu, inc - w, l);
+                        before += ex;
+                        cstar = c0 + l;
+                        break;
+                    }
+                    before += __shfl_sync(0xffffffffu, inc, 31);
+                }
+                // the crossing CTA's ids, in id order
+                const float invT = 1.0f / P->temperature;
+                const float *z = P->logits + P->V;
+                // CTA c holds tile groups [G8 c / nc, G8 (c + 1) / nc) of 8 ids each
+                const int i0 = 8 * (int)((long long)G8 * cstar / nc);
+                const int i1 = min(P->V, 8 * (int)((long long)G8 * (cstar + 1) / nc));
+                int pick = -1, lastnz = -1;
+                for (int b0 = i0; b0 < i1 && pick < 0; b0 += 32) {
+                    const int i = b0 + lane;
+                    const float w = i < i1 ? expf(z[i] * invT - M) : 0.f;
+                    float inc = w;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, inc, o);
+                        if (lane >= o) inc += y;
+                    }
+                    const unsigned hit = __ballot_sync(0xffffffffu, i < i1 && w > 0.f && before + inc > target);
+                    const unsigned nz = __ballot_sync(0xffffffffu, i < i1 && w > 0.f);
+                    if (nz) lastnz = b0 + 31 - __clz(nz);
+                    if (hit) pick = b0 + __ffs(hit) - 1;
+                    before += __shfl_sync(0xffffffffu, inc, 31);
+                }
+                if (lane == 0) P->st->samp = pick >= 0 ? pick : (lastnz >= 0 ? lastnz : min(i0, P->V - 1));
+            }
         }
     }
     if (tid == 0) *P->lm_cnt = 0;
@@ -468,9 +555,9 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // bulk copies (the projection's per anchor, masked ones zeroed instead); the
     // register-resident fragments are then read from there
     constexpr bool BULK = ESZ == 2;
-    // x rows in shared memory: rows 0..n the hi parts, rows n+1..2n+1 the lo parts (bf16,
-    // except for the LM head, whose four rows carry both parts already)
-    constexpr bool HILO = ESZ == 2 && OP != OP_LM;
+    // x rows in shared memory: rows 0..n, then for the projection (bf16) rows n+1..2n+1 with
+    // the lo parts (the LM head's four rows carry both parts of its two rows already)
+    constexpr bool HILO = ESZ == 2 && pg_hilo<OP>();
     const int xrows = OP == OP_LM ? 4 : (HILO ? 2 : 1) * (P->n + 1);
     const int xbytes = pg_xbytes(xrows, kx, ESZ);
     unsigned char *xs = smem;
@@ -540,7 +627,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     } else if constexpr (BULK) {
         if (tid == 0) {
             const __nv_bfloat16 *src = OP == OP_OPROJ ? P->ATTb : OP == OP_DOWN ? P->GUb : OP == OP_LM ? P->Xlm : P->Xb;
-            const long long lo = (long long)(P->n + 1) * K;   // the rows' lo parts follow the hi parts
+            const long long lo = (long long)(P->n + 1) * K;   // lo parts (if any) follow the hi parts
             const uint32_t rb = (uint32_t)kw * 2;
             fence_proxy_async();
             mbar_expect_tx(xbar, rb * R * (HILO ? 2 : 1));
@@ -585,7 +672,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     uint32_t tile = 0;
     int buf = 0;
     // LM head: this thread's argmax candidate and the draft row's logits for sampling
-    float lbv = -INFINITY;
+    float lbv = -INFINITY, lsm = -INFINITY, lss = 0.f;   // argmax; softmax statistics at T > 0
     int lbi = 0x7fffffff;
     float *dl = nullptr;
     if (OP == OP_LM && P->temperature > 0.f) dl = P->dlogits + (long long)ring(P->st->head + 1, 0, P->n + 1) * P->V;
@@ -607,8 +694,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
             if constexpr (ESZ == 2 && MT == 1) {
                 if (xreg) {
                     // one piece per tile (nch == 1): block bb = warp + 8j uses the j-th registers
-                    // for the hi parts; the lo parts (not for the LM head, whose four rows hold
-                    // both parts already) come from shared memory
+                    // for the hi parts; lo parts, where the GEMM has them, come from shared memory
                     const unsigned char *wp = tb + gq * rowb + tq * 16;
                     const unsigned char *lp = xlo + gq * xpitch + tq * 16;
                     const bool l0 = gq < R, l1 = gq + 8 < R;
@@ -731,6 +817,15 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
                         lbv = z;
                         lbi = row;
                     }
+                    if (P->lm_stats) {
+                        const float v = z / P->temperature;
+                        if (v > lsm) {
+                            lss = lss * expf(lsm - v) + 1.f;
+                            lsm = v;
+                        } else {
+                            lss += expf(v - lsm);
+                        }
+                    }
                 }
             } else if (ns == 1) {
                 pg_finish<T, OP>(P, pr, layer, g, xr_t, row, wr_t, s, xr_t < R, s_inv, pre);
@@ -741,7 +836,7 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
         buf ^= 1;
     }
     if constexpr (OP == OP_LM) {
-        pg_lm_argmax(P, xr_t, wr_t, lbv, lbi);
+        pg_lm_argmax(P, xr_t, wr_t, lbv, lbi, lsm, lss, G8);
         return;
     }
     if (ns == 1) return;

@@ -47,7 +47,7 @@ def test_struct_layouts_match_the_c_compiler(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     structs = [B.spd_dims, B.spd_layer_weights, B.spd_target_weights, B.spd_pdm_weights, B.spd_config,
-               B.spd_stats, B.spd_trace_rec]
+               B.spd_stats, B.spd_trace_rec, B.spd_trace_view]
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "spd.h"', 'int main(void){']
     for st in structs:
         lines.append(f'printf("%zu\\n", sizeof({st.__name__}));')

@@ -311,3 +311,38 @@ def test_bad_stage_bounds_are_refused():
         with pytest.raises(B.SPDError) as e:
             engine(SMALL, n=len(bounds) - 1, bounds=bounds)
         assert e.value.code == B.SPD_EINVAL
+
+
+def test_trace_view_is_the_device_copy_of_the_trace():
+    """spd_get_trace_view hands out the device records and KV lengths that spd_get_trace copies."""
+    import ctypes as C
+    from speculative_pipeline_decoding_spd_gb300 import binding as B
+    tg, pd, prompt, m, _, _ = materialise(SMALL)
+    e = engine(SMALL)
+    e.generate(torch.from_numpy(prompt).cuda())
+    tr = e.trace()
+    v = B.spd_get_trace_view(e.h)
+    assert v.count == len(tr) and v.L == SMALL.dm.L
+    lib = B.load()   # the CUDA runtime the library links resolves through its handle
+    lib.cudaMemcpy.argtypes = [C.c_void_p, C.c_void_p, C.c_size_t, C.c_int]
+    recs = (B.spd_trace_rec * v.count)()
+    lens = np.zeros((v.count, v.L), dtype=np.int32)
+    assert lib.cudaMemcpy(C.addressof(recs), v.recs, C.sizeof(recs), 2) == 0
+    assert lib.cudaMemcpy(lens.ctypes.data, v.kv_len, lens.nbytes, 2) == 0
+    e.close()
+    for r, g, ln in zip(tr, recs, lens):
+        assert (r["t"], r["exit_pos"], r["commit"], r["new_draft"]) == (g.t, g.exit_pos, g.commit, g.new_draft)
+        assert r["len"] == ln.tolist()
+
+
+@pytest.mark.parametrize("case", [SMALL, HD128, TINY], ids=["small", "hd128", "tiny"])
+def test_sampling_replay(case):
+    """T = 1: drafts sampled from the draft module's softmax, speculative rejection sampling with
+    residual resamples, on the same Philox uniforms as the oracle.  bf16 cases draw the draft
+    inside the tensor-core LM head (its softmax statistics merged across CTAs); the fp32 case
+    in the verification kernel."""
+    toks, tr, st, pf = run_gpu(case, temperature=1.0, seed=3)
+    o, rep = replay_oracle(case, tr, toks, temperature=1.0, seed=3)
+    compare(case, tr, o, rep)
+    assert o.tokens[case.prompt_len:] == toks
+    assert sum(1 for r in tr if r["accept"] == 0) > 0 and sum(1 for r in tr if r["accept"] == 1) > 0

@@ -215,6 +215,8 @@ def test_replay_argmax_adopts_only_near_ties():
     z[7] = 4.85                                 # now 0.15 below the top: outside the tolerance
     assert rep.pick_argmax(z, 7, "t", 4) == 3 and len(rep.mismatches) == 2
     assert rep.decisions == 4
+    assert rep.decisions_by == {"argmax": 4, "sample": 0, "keep": 0}
+    assert rep.adopted_by == {"argmax": 1, "sample": 0, "keep": 0}
     # no other side: the oracle's own pick, not counted as a decision
     assert rep.pick_argmax(z, None, "t", 5) == 3 and rep.decisions == 4
 
@@ -239,6 +241,7 @@ def test_replay_sample_adopts_only_the_neighbour_across_a_boundary():
     assert rep.pick_sample(w0, 0.3 - 5e-5, 1, "s", 8) == 0
     assert rep.pick_sample(w0, 0.3 - 5e-5, 9, "s", 9) == 0
     assert len(rep.mismatches) == 6 and rep.adopted == 2
+    assert rep.adopted_by["sample"] == 2 and rep.decisions_by["sample"] == 9
 
 
 def test_replay_keep_adopts_only_near_the_ratio():
