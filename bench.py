@@ -414,10 +414,11 @@ def main():
                      "traffic": None if traffic is None else round(traffic), "peak_kind": f"hbm_gbs ({pk_kind})",
                      "launches": r["gate_launches"]},
         "clocks": r["clocks"],
-        "e2e": {"value": round(r["e2e_tokens"] / r["e2e_s"], 2), "unit": "generated tokens/s (prefill + decode, "
-                "host buffers)", "h2d_bytes_per_step": round(4 * r["prompt_len"] / r["e2e_steps"], 3),
-                "d2h_bytes_per_step": round((4 * WL.max_new + 32 * math.ceil(r["e2e_steps"] / 8)) / r["e2e_steps"], 3),
-                "call": "spd_generate"},
+        "e2e": None if args.skip_e2e else {
+            "value": round(r["e2e_tokens"] / r["e2e_s"], 2), "unit": "generated tokens/s (prefill + decode, "
+            "host buffers)", "h2d_bytes_per_step": round(4 * r["prompt_len"] / r["e2e_steps"], 3),
+            "d2h_bytes_per_step": round((4 * WL.max_new + 32 * math.ceil(r["e2e_steps"] / 8)) / r["e2e_steps"], 3),
+            "call": "spd_generate"},
         "gpu_launches": r["launches_per_step"] * args.steps,
     }
     if ws == 1 and not args.no_cpu_baseline:

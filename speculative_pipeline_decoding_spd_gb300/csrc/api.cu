@@ -146,10 +146,10 @@ static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base,
     h.QKVp = b.take<float>((size_t)ns * qkv);
     h.ATTp = b.take<float>((size_t)ns * qr);
     h.GUp = b.take<float>((size_t)ns * d->F);
-    // bf16 input rows of the draft GEMMs (the anchors: hi parts, then lo parts)
-    h.Xb = b.take<__nv_bfloat16>((size_t)ns * d->d);
-    h.ATTb = b.take<__nv_bfloat16>((size_t)ns * qr);
-    h.GUb = b.take<__nv_bfloat16>((size_t)ns * d->F);
+    // bf16 input rows of the draft GEMMs: hi parts, then lo parts of the same size
+    h.Xb = b.take<__nv_bfloat16>((size_t)2 * ns * d->d);
+    h.ATTb = b.take<__nv_bfloat16>((size_t)2 * ns * qr);
+    h.GUb = b.take<__nv_bfloat16>((size_t)2 * ns * d->F);
     h.Xlm = b.take<__nv_bfloat16>((size_t)4 * d->d);
     h.ANCHb = b.take<__nv_bfloat16>((size_t)2 * ns * c->n_anchors * d->d);
     h.ssp = b.take<float>((size_t)MAXS * (d->d / 8));

@@ -88,13 +88,19 @@ struct AttnArgs {
                              // no merge here, every chunk (even a single one) leaves its partial
     int prob, maxch, Hq, Hkv, hd;
     float scale;
-    __nv_bfloat16 *outb;     // if set, the output goes here as bf16 instead of to out
+    __nv_bfloat16 *outb;     // if set, the output goes here as two bf16 parts instead of to out:
+    long long outb_lo;       // hi at outb[i], lo (what hi left out) at outb[outb_lo + i]
 };
 
 template <typename T>
 __device__ __forceinline__ void attn_store_out(const AttnArgs<T> &a, long long i, float v) {
-    if (a.outb) a.outb[i] = __float2bfloat16_rn(v);
-    else a.out[i] = v;
+    if (a.outb) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        a.outb[i] = hi;
+        a.outb[a.outb_lo + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+    } else {
+        a.out[i] = v;
+    }
 }
 
 // The work of CTA (kv head g, chunk c) for one problem, plus the merge when this CTA is

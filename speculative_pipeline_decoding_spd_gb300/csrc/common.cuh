@@ -98,12 +98,13 @@ struct Plan {
     long long lm_bytes;            // LM head per step
     float *Xp, *QKVp, *ATTp, *GUp;  // draft module rows: residual, q|k|v, attention, SiLU(gate)*up
     float *ssp;                    // [MAXS][d / 8] sums of squares of 8-row groups of the Xp rows
-    // bf16 weights: the draft GEMMs' inputs as bf16 rows, copied into shared memory whole
-    __nv_bfloat16 *Xb;             // [n+1][d] Xp * g of the next normalisation (1/rms applied after the GEMM)
-    __nv_bfloat16 *ATTb;           // [n+1][Hq hd] attention output
-    __nv_bfloat16 *GUb;            // [n+1][F] SiLU(gate) * up
-    __nv_bfloat16 *ANCHb;          // 2 x [n+1][nB][d] the anchor states (the draft projection's input):
-                                   // hi parts bf16(x), then (same layout, right after) lo parts bf16(x - hi)
+    // bf16 weights: the draft GEMMs' inputs as bf16 rows, copied into shared memory whole; each
+    // buffer holds the rows' hi parts bf16(x), then (same layout, right after) their lo parts
+    // bf16(x - hi)
+    __nv_bfloat16 *Xb;             // 2 x [n+1][d] Xp * g of the next normalisation (1/rms applied after the GEMM)
+    __nv_bfloat16 *ATTb;           // 2 x [n+1][Hq hd] attention output
+    __nv_bfloat16 *GUb;            // 2 x [n+1][F] SiLU(gate) * up
+    __nv_bfloat16 *ANCHb;          // 2 x [n+1][nB][d] the anchor states (the draft projection's input)
     __nv_bfloat16 *Xlm;            // [4][d] LM head rows: x * g_final of the exiting token and of the draft's newest row
                                    // (rows 0, 1: bf16 of the value; rows 2, 3: bf16 of what rows 0, 1 left out)
     float *pdm_part;               // draft GEMM K-slab partials [slab][n+1][N]

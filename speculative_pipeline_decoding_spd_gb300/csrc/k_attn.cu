@@ -79,9 +79,13 @@ __global__ void __launch_bounds__(ATT_THREADS, att_min_blocks<KvT<T>>()) k_attn(
         a.rope = nullptr;
         a.kraw = nullptr;
         a.vraw = nullptr;
-        // bf16 weights: the O GEMM copies its input rows as bf16
-        if (sizeof(T) == 2) a.outb = P->ATTb + (long long)s_src * P->q_rows;
-        else a.out = P->ATTp + (long long)s_src * P->q_rows;
+        // bf16 weights: the O GEMM copies its input rows as two bf16 parts
+        if (sizeof(T) == 2) {
+            a.outb = P->ATTb + (long long)s_src * P->q_rows;
+            a.outb_lo = (long long)(P->n + 1) * P->q_rows;
+        } else {
+            a.out = P->ATTp + (long long)s_src * P->q_rows;
+        }
         a.part = P->patt_part;
         a.cnt = P->patt_cnt;
         a.prob = s_src;

@@ -50,9 +50,8 @@ void pdm_plan(int d, int F, int q_rows, int nB, int n, int dtype, int kx[6], int
     *MT = rows <= 16 ? 1 : 2;
     const int Ks[6] = {nB * d, d, q_rows, d, F, d};
     for (int i = 0; i < 6; ++i) {
-        // bf16: the projection's rows as two bf16 parts each (the LM head: two rows, each as
-        // two parts)
-        kx[i] = pg_slab(Ks[i], i == OP_LM ? 4 : (esz == 2 && i == OP_PROJ ? 2 * rows : rows), esz);
+        // bf16: every row as two bf16 parts (the LM head: two rows, each as two parts)
+        kx[i] = pg_slab(Ks[i], i == OP_LM ? 4 : (esz == 2 ? 2 * rows : rows), esz);
         ns[i] = (Ks[i] + kx[i] - 1) / kx[i];
     }
 }

@@ -17,16 +17,19 @@
 
 namespace spd {
 
-constexpr int VT = 256;   // verify kernel threads
+constexpr int VT = 512;   // verify kernel threads
 
 __device__ __forceinline__ float u01(uint32_t w) { return (float)(w >> 8) * (1.0f / 16777216.0f); }
 
 // Block-wide inverse-CDF draw over weights w(i), i in [0, V): the smallest i whose running
 // sum (index order) exceeds u * total.  The ids are cut into tiles of 512 (16 per lane of a
-// warp): pass 1, each warp sums its tiles (tiles w, w + 8, ...; lane l reads ids l, l + 32,
+// warp): pass 1, each warp sums its tiles (tiles w, w + nw, ...; lane l reads ids l, l + 32,
 // ..., coalesced) with no block-wide barrier inside the loop; warp 0 then runs the running
 // sum over the tile totals in tile order (32 tiles per warp-wide scan), and scans the
 // crossing tile again with lane l owning the contiguous slice [16 l, 16 l + 16).
+// The weight functor has two parts, ld(i) (the global loads id i needs, as a float2) and
+// w(f) (the arithmetic): a lane issues all 16 loads of a tile before it computes any weight,
+// so a tile costs one memory latency, not sixteen.
 // Returns the index in all threads; *total_out receives the total.
 constexpr int SAMPLE_PER = 16;
 constexpr int SAMPLE_TILE = 32 * SAMPLE_PER;
@@ -42,23 +45,42 @@ __device__ __forceinline__ float warp_incl_scan(float v) {
     return v;
 }
 
+// weight exp(z_i / T - m) of a softmax draw (m the row's max of z / T)
+struct SoftmaxW {
+    const float *z;
+    float invT, m;
+    __device__ __forceinline__ float2 ld(int i) const { return make_float2(z[i], 0.f); }
+    __device__ __forceinline__ float w(float2 f) const { return expf(f.x * invT - m); }
+};
+// weight max(0, p_T(i) - p_D(i)) of the residual draw; rt, rd the reciprocals of the two
+// rows' sums of exp(z / T - max)
+struct ResidualW {
+    const float *zt, *zd;
+    float invT, mt, rt, md, rd;
+    __device__ __forceinline__ float2 ld(int i) const { return make_float2(zt[i], zd[i]); }
+    __device__ __forceinline__ float w(float2 f) const {
+        return fmaxf(expf(f.x * invT - mt) * rt - expf(f.y * invT - md) * rd, 0.f);
+    }
+};
+
 template <typename WF>
-__device__ int block_sample(int V, float u, WF wf, float *red, float *total_out) {
+__device__ int block_sample(int V, float u, const WF &wf, float *red, float *total_out) {
     __shared__ float s_tile[SAMPLE_MAX_TILES];
     __shared__ int s_pick;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int ntiles = (V + SAMPLE_TILE - 1) / SAMPLE_TILE;
     for (int t = warp; t < ntiles; t += nw) {
         const int base = t * SAMPLE_TILE;
-        float v[SAMPLE_PER];
+        float2 f[SAMPLE_PER];
 #pragma unroll
         for (int j = 0; j < SAMPLE_PER; ++j) {
             const int i = base + j * 32 + lane;
-            v[j] = i < V ? wf(i) : 0.f;
+            f[j] = i < V ? wf.ld(i) : make_float2(0.f, 0.f);
         }
         float loc = 0.f;
 #pragma unroll
-        for (int j = 0; j < SAMPLE_PER; ++j) loc += v[j];
+        for (int j = 0; j < SAMPLE_PER; ++j)
+            if (base + j * 32 + lane < V) loc += wf.w(f[j]);
         loc = warp_sum(loc);
         if (lane == 0) s_tile[t] = loc;
     }
@@ -94,10 +116,13 @@ __device__ int block_sample(int V, float u, WF wf, float *red, float *total_out)
         }
         // the crossing tile, lane l owning ids [16 l, 16 l + 16) of it
         const int lo = ct * SAMPLE_TILE + lane * SAMPLE_PER;
+        float2 f[SAMPLE_PER];
         float w[SAMPLE_PER], sl = 0.f;
 #pragma unroll
+        for (int j = 0; j < SAMPLE_PER; ++j) f[j] = lo + j < V ? wf.ld(lo + j) : make_float2(0.f, 0.f);
+#pragma unroll
         for (int j = 0; j < SAMPLE_PER; ++j) {
-            w[j] = lo + j < V ? wf(lo + j) : 0.f;
+            w[j] = lo + j < V ? wf.w(f[j]) : 0.f;
             sl += w[j];
         }
         const float inc = warp_incl_scan(sl);
@@ -160,19 +185,46 @@ __device__ void embed_into_slot(const Plan *__restrict__ P, int slot, int tok) {
     float *a0 = P->ANCH + (long long)slot * P->nB * d;
     __nv_bfloat16 *b0 = P->ANCHb + (long long)slot * P->nB * d;
     const long long blo = (long long)(P->n + 1) * P->nB * d;   // lo parts (zero: an embedding row is bf16)
-    for (int k = threadIdx.x; k < d; k += blockDim.x) {
-        const float v = WTraits<T>::get(e, k);
-        x[k] = v;
-        a0[k] = v;
-        if (sizeof(T) == 2) {
-            b0[k] = __float2bfloat16_rn(v);
-            b0[blo + k] = __float2bfloat16_rn(0.f);
+    // 8 elements per thread and pass: one 16-byte load of a bf16 row (two of an fp32 row), all
+    // of a thread's loads issued before its stores (d is a multiple of 64)
+    for (int k0 = 8 * threadIdx.x; k0 < d; k0 += 8 * blockDim.x) {
+        float v[8];
+        if constexpr (sizeof(T) == 2) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(e + k0);
+            v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+            v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+            *reinterpret_cast<uint4 *>(b0 + k0) = w;                               // the hi parts are the row itself
+            *reinterpret_cast<uint4 *>(b0 + blo + k0) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            const float4 f0 = *reinterpret_cast<const float4 *>(e + k0);
+            const float4 f1 = *reinterpret_cast<const float4 *>(e + k0 + 4);
+            v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w; v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
         }
+        const float4 o0 = make_float4(v[0], v[1], v[2], v[3]), o1 = make_float4(v[4], v[5], v[6], v[7]);
+        *reinterpret_cast<float4 *>(x + k0) = o0;
+        *reinterpret_cast<float4 *>(x + k0 + 4) = o1;
+        *reinterpret_cast<float4 *>(a0 + k0) = o0;
+        *reinterpret_cast<float4 *>(a0 + k0 + 4) = o1;
+    }
+}
+
+// The plan's scalars and buffer pointers (all of it but the per-layer weight tables, which the
+// verify kernel does not read) copied into shared memory by all threads in one round of loads,
+// so that thread 0's decisions below wait on no global load of their own.
+__device__ void plan_to_shared(const Plan *g, Plan *s) {
+    static_assert(offsetof(Plan, tl) % 4 == 0 && offsetof(Plan, X) % 4 == 0 && sizeof(Plan) % 4 == 0, "word copy");
+    constexpr int h = (int)(offsetof(Plan, tl) / 4), t0 = (int)(offsetof(Plan, X) / 4), e = (int)(sizeof(Plan) / 4);
+    const int *src = reinterpret_cast<const int *>(g);
+    int *dst = reinterpret_cast<int *>(s);
+    for (int i = threadIdx.x; i < h + (e - t0); i += blockDim.x) {
+        const int w = i < h ? i : t0 + (i - h);
+        dst[w] = src[w];
     }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
+__global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ Pg) {
+    __shared__ __align__(16) Plan sP;
     __shared__ float red[40];
     __shared__ int s_done, s_t, s_head, s_ex, s_q, s_x, s_xslot, s_P0, s_newslot, s_draft, s_y, s_ok, s_active;
     __shared__ float s_tmax, s_tsum;
@@ -182,13 +234,16 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
     __shared__ __align__(16) DevState sst;
     __shared__ int s_err0;
     static_assert(sizeof(DevState) % 16 == 0, "state copied in 16-byte words");
-    const int n = P->n, ns = n + 1, V = P->V;
-    const float T_ = P->temperature;
+    plan_to_shared(Pg, &sP);   // the plan does not change during a step: read before the wait
+    DevState *const gst = Pg->st;
     pdl_wait();   // logits and argmax of the LM head launch
     pdl_trigger();
     for (int i = threadIdx.x; i < (int)(sizeof(DevState) / 16); i += blockDim.x)
-        reinterpret_cast<uint4 *>(&sst)[i] = reinterpret_cast<const uint4 *>(P->st)[i];
+        reinterpret_cast<uint4 *>(&sst)[i] = reinterpret_cast<const uint4 *>(gst)[i];
     __syncthreads();
+    const Plan *P = &sP;
+    const int n = P->n, ns = n + 1, V = P->V;
+    const float T_ = P->temperature;
     DevState *st = &sst;
     if (threadIdx.x == 0) {
         s_err0 = st->error;
@@ -265,7 +320,7 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
             float m, s;
             softmax_stats(zd, V, invT, red, &m, &s);
             const float u0 = u01(philox_word0((uint32_t)t, 0u, P->seed_lo, P->seed_hi));
-            const int pick = block_sample(V, u0, [&](int i) { return expf(zd[i] * invT - m); }, red + 4, nullptr);
+            const int pick = block_sample(V, u0, SoftmaxW{zd, invT, m}, red + 4, nullptr);
             if (threadIdx.x == 0) {
                 s_draft = pick;
                 st->dmax[s_newslot] = m;
@@ -310,13 +365,8 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
                 const float tmx = s_tmax, tsm = s_tsum;
                 const float u2 = u01(philox_word0((uint32_t)t, 2u, P->seed_lo, P->seed_hi));
                 float tot;
-                auto resid = [&](int i) {
-                    const float pt = expf(zt[i] * invT - tmx) / tsm;
-                    const float pd = expf(zd[i] * invT - dm) / ds;
-                    return fmaxf(pt - pd, 0.f);
-                };
-                int y = block_sample(V, u2, resid, red + 4, &tot);
-                if (!(tot > 0.f)) y = block_sample(V, u2, [&](int i) { return expf(zt[i] * invT - tmx); }, red + 4, nullptr);
+                int y = block_sample(V, u2, ResidualW{zt, zd, invT, tmx, 1.0f / tsm, dm, 1.0f / ds}, red + 4, &tot);
+                if (!(tot > 0.f)) y = block_sample(V, u2, SoftmaxW{zt, invT, tmx}, red + 4, nullptr);
                 if (threadIdx.x == 0) s_y = y;
             } else if (threadIdx.x == 0) {
                 s_y = s_x;
@@ -427,7 +477,7 @@ __global__ void __launch_bounds__(VT) k_prefill_finalize(const Plan *__restrict_
         float m, s;
         softmax_stats(z, V, invT, red, &m, &s);
         const float u = u01(philox_word0(0u, 2u, P->seed_lo, P->seed_hi));
-        const int y = block_sample(V, u, [&](int i) { return expf(z[i] * invT - m); }, red + 4, nullptr);
+        const int y = block_sample(V, u, SoftmaxW{z, invT, m}, red + 4, nullptr);
         if (threadIdx.x == 0) s_y = y;
     } else {
         float bv = -INFINITY;

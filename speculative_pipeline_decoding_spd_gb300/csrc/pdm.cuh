@@ -8,13 +8,13 @@
 // tokens, at consecutive positions.
 //
 // Every GEMM here multiplies one weight matrix W [N][K] by R <= n+1 row vectors x [R][K]
-// (far more bytes of W than of x: bound by streaming W once from HBM).  With bf16 weights the
-// projection's input (the concatenated anchors) arrives as two bf16 rows per row, hi = bf16(x)
-// and lo = bf16(x - hi), and both meet the weights on the tensor cores (the products add up
-// in the same accumulators), so the projection sees its input at about 16 mantissa bits.  Its
-// rounding dominates the module's: in fp64 on the 4B shape, rounding only the projection's
-// input to bf16 moves the draft logits by 7.5e-3 of their scale, any one of the layers'
-// GEMM inputs by 0.3e-3 to 2.1e-3.  A group of CTAs does one GEMM; per CTA:
+// (far more bytes of W than of x: bound by streaming W once from HBM).  With bf16 weights
+// each x row arrives as two bf16 rows, hi = bf16(x) and lo = bf16(x - hi), and both meet the
+// weights on the tensor cores (the products add up in the same accumulators), so the GEMM
+// sees x at about 16 mantissa bits, not 8.  (In fp64 on the 4B shape over 8 decode steps,
+// rounding one kind of input to bf16 moves the newest row's draft logits by 1.7e-2 (gate/up),
+// 1.6e-2 (O), 1.3e-2 (down), 3.8e-3 (QKV), 0.7e-3 (projection); all of them 2.7e-2.)  A group
+// of CTAs does one GEMM; per CTA:
 //   * a producer warp streams 8-row tiles of W (each row piece up to 6 KB, 1-D bulk
 //     copies) into a shared-memory ring signalled by mbarriers;
 //   * the R rows of x for the CTA's K slab go to shared memory: for bf16 weights the kernel
@@ -140,8 +140,16 @@ __device__ __forceinline__ PgRows<T, OP> pg_rows(const Plan *__restrict__ P, int
     return r;
 }
 
-// Draft GEMMs whose bf16 input rows come as hi and lo parts (the projection's anchors).
-template <int OP> __host__ __device__ constexpr bool pg_hilo() { return OP == OP_PROJ; }
+// Draft GEMMs whose bf16 input rows come as hi and lo parts: all but the LM head (whose four
+// rows carry both parts of its two rows already).
+template <int OP> __host__ __device__ constexpr bool pg_hilo() { return OP != OP_LM; }
+
+// bf16 input row element in two parts: hi at p[i], lo (what hi left out) at p[lo_off + i]
+__device__ __forceinline__ void store_hilo(__nv_bfloat16 *p, long long lo_off, long long i, float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    p[i] = hi;
+    p[lo_off + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
 
 // ---- x staging (consumer warps only) ---------------------------------------------------
 template <typename XT>
@@ -281,7 +289,7 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
         const float up = __shfl_xor_sync(0xffffffffu, v, 8);
         if (valid && wr < 4) {
             const float h = silu_f(v) * up;
-            if (sizeof(T) == 2) P->GUb[(long long)xr * P->F + row] = __float2bfloat16_rn(h);
+            if (sizeof(T) == 2) store_hilo(P->GUb, (long long)(P->n + 1) * P->F, (long long)xr * P->F + row, h);
             else P->GUp[(long long)xr * P->F + row] = h;
         }
     } else {
@@ -292,7 +300,8 @@ __device__ __forceinline__ void pg_finish(const Plan *__restrict__ P, const PdmR
             // bf16 input row of the next GEMM: x * g of its normalisation; after the last layer
             // the newest row is the LM head's second input row
             if (sizeof(T) == 2) {
-                if (OP != OP_DOWN || layer + 1 < P->Ls) P->Xb[(long long)xr * P->d + row] = __float2bfloat16_rn(o * pre.y);
+                if (OP != OP_DOWN || layer + 1 < P->Ls)
+                    store_hilo(P->Xb, (long long)(P->n + 1) * P->d, (long long)xr * P->d + row, o * pre.y);
                 else if (xr == pr.R - 1) {
                     // the LM head's second input row in two bf16 parts: the value and the rest
                     const float xl = o * pre.y;
@@ -555,8 +564,8 @@ __device__ void pdm_gemm_cta(const Plan *__restrict__ P, const PdmRows &pr, int 
     // bulk copies (the projection's per anchor, masked ones zeroed instead); the
     // register-resident fragments are then read from there
     constexpr bool BULK = ESZ == 2;
-    // x rows in shared memory: rows 0..n, then for the projection (bf16) rows n+1..2n+1 with
-    // the lo parts (the LM head's four rows carry both parts of its two rows already)
+    // x rows in shared memory: rows 0..n the hi parts, rows n+1..2n+1 the lo parts (bf16, but
+    // not the LM head, whose four rows carry both parts of its two rows already)
     constexpr bool HILO = ESZ == 2 && pg_hilo<OP>();
     const int xrows = OP == OP_LM ? 4 : (HILO ? 2 : 1) * (P->n + 1);
     const int xbytes = pg_xbytes(xrows, kx, ESZ);

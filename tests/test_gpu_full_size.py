@@ -12,9 +12,9 @@ the GPU only at near-ties).  Every workload starts from its own full prompt:
 On top of the traces, the first steps of configs 2 to 5 compare vectors: logits entry by
 entry, the draft block's rows, residual streams, anchors and the K/V rows written.
 
-With SPD_LONG_PARITY=1 the prefixes become whole generations: config 3 in every mode to 512
-tokens (p = 0.6 about 3100 steps, greedy about 4100) and config 5 to 1024 tokens.  Those take
-the oracle about an hour on 16 host cores, so they are opt-in.
+With SPD_LONG_PARITY=1 config 3's forced p = 0.6 and greedy runs go to their 512th token
+(about 2000 and 4100 steps), and config 5 to its 1024th.  The oracle needs about 0.35 s a step
+at the 4B shape on 16 host cores, so those are opt-in.
 
 Forced drafts follow the oracle's own greedy stream, so no oracle input comes from the GPU.
 Each workload is built once: weights drawn on the host from the seeded generators and
@@ -145,14 +145,13 @@ def test_config2_06b_whole_generation():
 
 def test_config3_4b_all_modes():
     """4B shape, n = 8, Ls = 4, prompt 512: forced p = 0.6, greedy drafting and p = 0.3 / 0.9
-    replayed over prefixes (whole 512-token generations with SPD_LONG_PARITY=1); vectors over
-    the first 8 steps."""
+    replayed over prefixes (p = 0.6 and greedy to the 512th token with SPD_LONG_PARITY=1);
+    vectors over the first 8 steps."""
     wl = si.SHAPE_4B
     case = case_of(wl)
     ref, _ = forced_ref(case, case.max_new)
     base = None
-    runs = [(0.6, None if LONG else 600), (None, None if LONG else 300), (0.3, None if LONG else 200),
-            (0.9, None if LONG else 200)]
+    runs = [(0.6, None if LONG else 600), (None, None if LONG else 300), (0.3, 200), (0.9, 200)]
     for p, steps in runs:
         kw = {} if p is None else dict(force_p=p, forced_ref=torch.from_numpy(ref).cuda(), seed=2)
         tr, toks = gpu_steps(case, steps, **kw)
