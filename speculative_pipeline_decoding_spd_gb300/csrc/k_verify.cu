@@ -208,23 +208,8 @@ __device__ void embed_into_slot(const Plan *__restrict__ P, int slot, int tok) {
     }
 }
 
-// The plan's scalars and buffer pointers (all of it but the per-layer weight tables, which the
-// verify kernel does not read) copied into shared memory by all threads in one round of loads,
-// so that thread 0's decisions below wait on no global load of their own.
-__device__ void plan_to_shared(const Plan *g, Plan *s) {
-    static_assert(offsetof(Plan, tl) % 4 == 0 && offsetof(Plan, X) % 4 == 0 && sizeof(Plan) % 4 == 0, "word copy");
-    constexpr int h = (int)(offsetof(Plan, tl) / 4), t0 = (int)(offsetof(Plan, X) / 4), e = (int)(sizeof(Plan) / 4);
-    const int *src = reinterpret_cast<const int *>(g);
-    int *dst = reinterpret_cast<int *>(s);
-    for (int i = threadIdx.x; i < h + (e - t0); i += blockDim.x) {
-        const int w = i < h ? i : t0 + (i - h);
-        dst[w] = src[w];
-    }
-}
-
 template <typename T>
-__global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ Pg) {
-    __shared__ __align__(16) Plan sP;
+__global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ P) {
     __shared__ float red[40];
     __shared__ int s_done, s_t, s_head, s_ex, s_q, s_x, s_xslot, s_P0, s_newslot, s_draft, s_y, s_ok, s_active;
     __shared__ float s_tmax, s_tsum;
@@ -234,14 +219,12 @@ __global__ void __launch_bounds__(VT) k_verify(const Plan *__restrict__ Pg) {
     __shared__ __align__(16) DevState sst;
     __shared__ int s_err0;
     static_assert(sizeof(DevState) % 16 == 0, "state copied in 16-byte words");
-    plan_to_shared(Pg, &sP);   // the plan does not change during a step: read before the wait
-    DevState *const gst = Pg->st;
+    DevState *const gst = P->st;
     pdl_wait();   // logits and argmax of the LM head launch
     pdl_trigger();
     for (int i = threadIdx.x; i < (int)(sizeof(DevState) / 16); i += blockDim.x)
         reinterpret_cast<uint4 *>(&sst)[i] = reinterpret_cast<const uint4 *>(gst)[i];
     __syncthreads();
-    const Plan *P = &sP;
     const int n = P->n, ns = n + 1, V = P->V;
     const float T_ = P->temperature;
     DevState *st = &sst;

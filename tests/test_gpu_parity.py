@@ -37,6 +37,11 @@ WIDEK = Case(si.ModelDims(L=32, d=2560, Hq=8, Hkv=2, hd=128, F=2560, V=1000), n=
 # bf16, 2 stages of 3 layers with 2 draft layers (more draft layers relative to the stages)
 INROUNDS = Case(si.ModelDims(L=6, d=512, Hq=8, Hkv=2, hd=64, F=1024, V=1600), n=2, anchors=(0, 3, 6), Ls=2,
                 prompt_len=200, max_new=48, norms="perturbed")
+# bf16, the 8B shape's width and heads (d 4096, 32q/8kv x 128) over 5 one-layer stages: 6 draft
+# rows (12 with their lo parts) split the draft QKV, O and gate/up into two K slabs, and the LM
+# head's 8 KB rows take two pieces per tile
+D4096 = Case(si.ModelDims(L=5, d=4096, Hq=32, Hkv=8, hd=128, F=2048, V=2048), n=5, anchors=(0, 2, 5), Ls=1,
+             prompt_len=64, max_new=32, norms="perturbed")
 # MULTI's draft projection (K = 5 x 2560) is split into K slabs across CTAs; its QKV, O, gate/up
 # and down keep x in registers (one 16-row tile, K <= 2560); WIDE's 17 rows keep x in shared memory.
 
@@ -223,6 +228,7 @@ VEC_CASES = [
     ("multi", MULTI, {}),
     ("wide-forced", WIDE, dict(p=0.7)),
     ("widek", WIDEK, {}),
+    ("d4096-forced", D4096, dict(p=0.6)),
     ("inrounds-forced", INROUNDS, dict(p=0.6)),
     ("small-output", SMALL, dict(speculate="output", p=0.6)),
     ("hd128-bounds", HD128, dict(bounds=(0, 1, 2, 4, 5), p=0.6)),
