@@ -28,8 +28,8 @@
  *     internal second stream joined back to it); calls return after issuing work,
  *     except where an argument named *_host receives a result (those synchronise).
  *   - Layout: matrices are row-major [out][in] in the dtype of spd_dims.dtype;
- *     norm gains are fp32 vectors.  KV caches are fp32 for fp32 weights and fp16 for
- *     bf16 weights (same bytes as bf16, 8x finer rounding; values saturate at +-65504).
+ *     norm gains are fp32 vectors.  The KV caches hold fp32 rows for every weight type
+ *     (the cache's rounding would otherwise reach every later token's logits).
  */
 #ifndef SPD_H
 #define SPD_H
@@ -50,8 +50,8 @@ extern "C" {
 #define SPD_ECAPACITY 5  /* max_seq, max_new or the step-trace capacity would overflow */
 #define SPD_EDEVICE 6    /* a kernel reported an error flag (bounds check failed)      */
 
-/* element types: weights are SPD_F32 or SPD_BF16; the KV caches of a handle are fp32 for
- * fp32 weights and fp16 (SPD_F16) for bf16 weights */
+/* element types: weights are SPD_F32 or SPD_BF16; the KV caches of a handle are fp32.
+ * SPD_F16 names an fp16 K/V operand of the stand-alone attention call below */
 #define SPD_F32 0
 #define SPD_BF16 1
 #define SPD_F16 2
@@ -257,7 +257,7 @@ int spd_get_tokens(spd_handle *h, int32_t *tokens_host, int32_t max_tokens, int3
 #define SPD_BUF_RESIDUAL 0   /* fp32 [n+1][d]: per-slot residual stream (slot ring)       */
 #define SPD_BUF_ANCHORS 1    /* fp32 [n+1][n_anchors][d]: per-slot anchor states          */
 #define SPD_BUF_LOGITS 2     /* fp32 [2][V]: last step's target-exit and draft logits     */
-#define SPD_BUF_KCACHE 3     /* KV type [max_seq][Hkv][hd] of target layer `index`       */
+#define SPD_BUF_KCACHE 3     /* fp32 [max_seq][Hkv][hd] of target layer `index`          */
 #define SPD_BUF_VCACHE 4
 #define SPD_BUF_PDM_KCACHE 5 /* same, draft layer `index`                                */
 #define SPD_BUF_PDM_VCACHE 6

@@ -42,7 +42,7 @@ struct spd_handle {
     int *host_pinned = nullptr;     // [8] small readback buffer
     size_t ws_bytes = 0;
     void *ws = nullptr;
-    int elem = 2;
+    int elem = 2;                   // bytes of a weight element
 };
 
 static int fail(spd_handle *H, int code, const std::string &msg) {
@@ -123,7 +123,7 @@ static void stage_plan(const spd_dims *d, const spd_config *c, int *b) {
 
 static size_t layout(const spd_dims *d, int Ls, const spd_config *c, char *base, Plan &h) {
     Bump b{base};
-    const int n = c->n, ns = n + 1, elem = d->dtype == SPD_BF16 ? 2 : 4;
+    const int n = c->n, ns = n + 1, elem = (int)sizeof(KvT<float>);   // KV cache elements (fp32)
     const int qkv = (d->Hq + 2 * d->Hkv) * d->hd, qr = d->Hq * d->hd;
     const int max_chunks = (c->max_seq + ATT_CHUNK - 1) / ATT_CHUNK;
     const int max_steps = n * c->max_new + 2 * n + 8;
@@ -667,7 +667,7 @@ extern "C" int spd_read_buffer(spd_handle *H, int32_t which, int32_t index, size
     const Plan &h = H->h;
     const char *src = nullptr;
     size_t size = 0;
-    const size_t kvb = (size_t)h.kv_stride * H->elem;
+    const size_t kvb = (size_t)h.kv_stride * sizeof(KvT<float>);   // one layer's cache (fp32 rows)
     switch (which) {
         case SPD_BUF_RESIDUAL: src = (const char *)h.X; size = (size_t)(h.n + 1) * h.d * 4; break;
         case SPD_BUF_ANCHORS: src = (const char *)h.ANCH; size = (size_t)(h.n + 1) * h.nB * h.d * 4; break;

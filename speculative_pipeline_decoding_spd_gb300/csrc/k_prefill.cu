@@ -233,17 +233,21 @@ __global__ void __launch_bounds__(256) k_pf_attn(const Plan *__restrict__ P, con
     }
 }
 
-// ---- causal attention of a prompt chunk on tensor cores (fp16 K/V cache) ------------------
-// CTA = 64 query rows of one query head (4 warps x 16 rows), flash-attention order: key
-// tiles of 64 positions staged in shared memory by cp.async (double buffered), scores
-// S = Q K^T by mma.sync m16n8k16 (q as two fp16 parts, hi and lo, so the scores see about
-// 21 bits of q; K as stored), an online softmax per row in registers, P rounded to fp16 and
-// O += P V by mma.sync; the causal mask applies on the diagonal tile only.  Output fp32
-// [row][Hq * hd], as the tensor-core O projection's input split expects.
+// ---- causal attention of a prompt chunk on tensor cores (fp32 K/V cache) ------------------
+// CTA = 64 query rows of one query head (4 warps x 16 rows), flash-attention order over key
+// tiles of 64 positions.  cp.async copies the next tile's fp32 K and V rows into a staging
+// buffer while the warps work on the current tile, which has been split into fp16 parts
+// hi = fp16(x) and lo = fp16(x - hi) (about 21 bits of each value).  Scores S = Q K^T by
+// mma.sync m16n8k16 as q_hi k_hi + q_lo k_hi + q_hi k_lo (q pre-scaled by 1/sqrt(hd) and split
+// the same way; the lo x lo term lies below the fp32 accumulation's resolution), an online
+// softmax per row in registers, the probabilities split the same way and
+// O += P_hi V_hi + P_lo V_hi + P_hi V_lo; the causal mask applies on the diagonal tile only.
+// Output fp32 [row][Hq * hd], as the tensor-core O projection's input split expects.
 constexpr int FA_BQ = 64, FA_BK = 64, FA_THREADS = 128;
 template <int HD> __host__ __device__ constexpr int fa_pitch() { return HD + 8; }   // halfs; ldmatrix rows on distinct banks
 template <int HD> __host__ __device__ constexpr int fa_smem_bytes() {
-    return (2 * FA_BQ + 4 * FA_BK) * fa_pitch<HD>() * 2;   // q hi, q lo, two stages of K and V
+    // q hi / lo, K hi / lo, V hi / lo (fp16 tiles), then the fp32 K and V staging rows
+    return (2 * FA_BQ + 4 * FA_BK) * fa_pitch<HD>() * 2 + 2 * FA_BK * HD * 4;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -266,13 +270,30 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// fp16 parts of four fp32 values: hi = fp16(x) (range-clamped), lo = fp16(x - hi)
+__device__ __forceinline__ void split_h4(const float4 v, __half *hi, __half *lo) {
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    __half h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[i] = __float2half_rn(fminf(fmaxf(x[i], -F16_MAX), F16_MAX));
+        l[i] = __float2half_rn(x[i] - __half2float(h[i]));
+    }
+    *reinterpret_cast<uint2 *>(hi) = make_uint2((uint32_t)__half_as_ushort(h[0]) | ((uint32_t)__half_as_ushort(h[1]) << 16),
+                                                (uint32_t)__half_as_ushort(h[2]) | ((uint32_t)__half_as_ushort(h[3]) << 16));
+    *reinterpret_cast<uint2 *>(lo) = make_uint2((uint32_t)__half_as_ushort(l[0]) | ((uint32_t)__half_as_ushort(l[1]) << 16),
+                                                (uint32_t)__half_as_ushort(l[2]) | ((uint32_t)__half_as_ushort(l[3]) << 16));
+}
+
 template <int HD>
 __global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P, const float *__restrict__ qkv, int p0,
-                                                      int M, const __half *__restrict__ kc, const __half *__restrict__ vc,
+                                                      int M, const float *__restrict__ kc, const float *__restrict__ vc,
                                                       float *__restrict__ out) {
-    extern __shared__ __align__(16) __half fa_s[];
+    extern __shared__ __align__(16) unsigned char fa_raw[];
     constexpr int PT = fa_pitch<HD>(), NT = FA_BK / 8, KS = HD / 16, NO = HD / 8;
-    __half *Qh = fa_s, *Ql = Qh + FA_BQ * PT, *Ks = Ql + FA_BQ * PT, *Vs = Ks + 2 * FA_BK * PT;
+    __half *Qh = reinterpret_cast<__half *>(fa_raw), *Ql = Qh + FA_BQ * PT;
+    __half *Kh = Ql + FA_BQ * PT, *Kl = Kh + FA_BK * PT, *Vh = Kl + FA_BK * PT, *Vl = Vh + FA_BK * PT;
+    float *Kf = reinterpret_cast<float *>(Vl + FA_BK * PT), *Vf = Kf + FA_BK * HD;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int h = blockIdx.y, G = P->Hq / P->Hkv, g = h / G;
     const int q0 = blockIdx.x * FA_BQ;
@@ -281,24 +302,34 @@ __global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P
     const int kend = min(kv_end, p0 + q0 + FA_BQ);              // keys any row of this CTA sees
     const int ntiles = (kend + FA_BK - 1) / FA_BK;
     const float scale = P->scale;
-    // ---- K / V tile loader (rows past the written keys are zero)
-    auto load_tile = [&](int t, int buf) {
+    // ---- fp32 K / V rows of tile t into the staging rows (rows past the written keys are zero)
+    auto stage_tile = [&](int t) {
         const int k0 = t * FA_BK;
-        for (int c = tid; c < FA_BK * HD / 8; c += FA_THREADS) {
-            const int j = c / (HD / 8), e = (c - j * (HD / 8)) * 8;
-            __half *kd = Ks + (buf * FA_BK + j) * PT + e;
-            __half *vd = Vs + (buf * FA_BK + j) * PT + e;
+        for (int c = tid; c < FA_BK * HD / 4; c += FA_THREADS) {
+            const int j = c / (HD / 4), e = (c - j * (HD / 4)) * 4;
+            float *kd = Kf + j * HD + e, *vd = Vf + j * HD + e;
             if (k0 + j < kv_end) {
                 cp_async16(kd, kc + (long long)(k0 + j) * rs + (long long)g * HD + e);
                 cp_async16(vd, vc + (long long)(k0 + j) * rs + (long long)g * HD + e);
             } else {
-                *reinterpret_cast<uint4 *>(kd) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(vd) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<float4 *>(kd) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(vd) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    load_tile(0, 0);
+    // ---- the staged rows as fp16 hi / lo tiles (after every thread's copies have landed)
+    auto split_tile = [&]() {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        for (int c = tid; c < FA_BK * HD / 4; c += FA_THREADS) {
+            const int j = c / (HD / 4), e = (c - j * (HD / 4)) * 4;
+            split_h4(*reinterpret_cast<const float4 *>(Kf + j * HD + e), Kh + j * PT + e, Kl + j * PT + e);
+            split_h4(*reinterpret_cast<const float4 *>(Vf + j * HD + e), Vh + j * PT + e, Vl + j * PT + e);
+        }
+        __syncthreads();
+    };
+    stage_tile(0);
     // ---- q (rotated already), pre-scaled by 1/sqrt(hd), as fp16 hi + lo
     for (int c = tid; c < FA_BQ * HD; c += FA_THREADS) {
         const int r = c / HD, e = c - r * HD;
@@ -308,6 +339,7 @@ __global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P
         Qh[r * PT + e] = hi;
         Ql[r * PT + e] = __float2half_rn(v - __half2float(hi));
     }
+    split_tile();
     float o[NO][4];
 #pragma unroll
     for (int i = 0; i < NO; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -317,19 +349,11 @@ __global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P
     const uint32_t qh_addr = smem_u32(Qh + (r0 + (lane & 15)) * PT + (lane >> 4) * 8);
     const uint32_t ql_addr = smem_u32(Ql + (r0 + (lane & 15)) * PT + (lane >> 4) * 8);
     for (int t = 0; t < ntiles; ++t) {
-        const int buf = t & 1;
-        if (t + 1 < ntiles) {
-            load_tile(t + 1, buf ^ 1);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-        }
-        __syncthreads();
+        if (t + 1 < ntiles) stage_tile(t + 1);   // the staging rows are free once split
         // ---- S = Q K^T: 16 rows x 64 keys per warp
         float sc[NT][4];
 #pragma unroll
         for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-        const __half *kb = Ks + buf * FA_BK * PT;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3;
@@ -337,14 +361,18 @@ __global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P
             ldsm_x4(ql_addr + ks * 32, al0, al1, al2, al3);
 #pragma unroll
             for (int np = 0; np < NT / 2; ++np) {
-                // keys 16 np .. 16 np + 15: two n8 tiles
-                uint32_t b0, b1, b2, b3;
+                // keys 16 np .. 16 np + 15: two n8 tiles, hi and lo parts
+                uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
                 const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                ldsm_x4(smem_u32(kb + key * PT + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1, b2, b3);
+                const int off = key * PT + ks * 16 + ((lane >> 3) & 1) * 8;
+                ldsm_x4(smem_u32(Kh + off), b0, b1, b2, b3);
+                ldsm_x4(smem_u32(Kl + off), c0, c1, c2, c3);
                 mma_f16(sc[2 * np], ah0, ah1, ah2, ah3, b0, b1);
                 mma_f16(sc[2 * np], al0, al1, al2, al3, b0, b1);
+                mma_f16(sc[2 * np], ah0, ah1, ah2, ah3, c0, c1);
                 mma_f16(sc[2 * np + 1], ah0, ah1, ah2, ah3, b2, b3);
                 mma_f16(sc[2 * np + 1], al0, al1, al2, al3, b2, b3);
+                mma_f16(sc[2 * np + 1], ah0, ah1, ah2, ah3, c2, c3);
             }
         }
         // ---- causal mask on the diagonal tile, online softmax
@@ -373,21 +401,21 @@ __global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P
         float corr[2], ls[2] = {0.f, 0.f};
 #pragma unroll
         for (int r = 0; r < 2; ++r) corr[r] = mx[r] == -INFINITY ? 1.f : expf(mrow[r] - mx[r]);
-        uint32_t pa[NT][2];
+        uint32_t ph[NT][2], pl[NT][2];
 #pragma unroll
         for (int i = 0; i < NT; ++i) {
             const float e0 = mx[0] == -INFINITY ? 0.f : expf(sc[i][0] - mx[0]);
             const float e1 = mx[0] == -INFINITY ? 0.f : expf(sc[i][1] - mx[0]);
             const float e2 = mx[1] == -INFINITY ? 0.f : expf(sc[i][2] - mx[1]);
             const float e3 = mx[1] == -INFINITY ? 0.f : expf(sc[i][3] - mx[1]);
-            // the row sums take the probabilities as rounded for the P V product
-            const uint32_t p01 = pack_h2(e0, e1), p23 = pack_h2(e2, e3);
-            const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&p01));
-            const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&p23));
-            ls[0] += f01.x + f01.y;
-            ls[1] += f23.x + f23.y;
-            pa[i][0] = p01;
-            pa[i][1] = p23;
+            ls[0] += e0 + e1;
+            ls[1] += e2 + e3;
+            const __half2 h01 = __floats2half2_rn(e0, e1), h23 = __floats2half2_rn(e2, e3);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            ph[i][0] = *reinterpret_cast<const uint32_t *>(&h01);
+            ph[i][1] = *reinterpret_cast<const uint32_t *>(&h23);
+            pl[i][0] = pack_h2(e0 - f01.x, e1 - f01.y);
+            pl[i][1] = pack_h2(e2 - f23.x, e3 - f23.y);
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -404,20 +432,27 @@ __global__ void __launch_bounds__(FA_THREADS) k_pf_fa(const Plan *__restrict__ P
             o[i][3] *= corr[1];
         }
         // ---- O += P V
-        const __half *vb = Vs + buf * FA_BK * PT;
 #pragma unroll
         for (int s = 0; s < FA_BK / 16; ++s) {
-            const uint32_t a0 = pa[2 * s][0], a1 = pa[2 * s][1], a2 = pa[2 * s + 1][0], a3 = pa[2 * s + 1][1];
+            const uint32_t a0 = ph[2 * s][0], a1 = ph[2 * s][1], a2 = ph[2 * s + 1][0], a3 = ph[2 * s + 1][1];
+            const uint32_t l0 = pl[2 * s][0], l1 = pl[2 * s][1], l2 = pl[2 * s + 1][0], l3 = pl[2 * s + 1][1];
 #pragma unroll
             for (int np = 0; np < NO / 2; ++np) {
-                uint32_t b0, b1, b2, b3;
+                uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
                 const int key = s * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                ldsm_x4_t(smem_u32(vb + key * PT + np * 16 + (lane >> 4) * 8), b0, b1, b2, b3);
+                const int off = key * PT + np * 16 + (lane >> 4) * 8;
+                ldsm_x4_t(smem_u32(Vh + off), b0, b1, b2, b3);
+                ldsm_x4_t(smem_u32(Vl + off), c0, c1, c2, c3);
                 mma_f16(o[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_f16(o[2 * np], l0, l1, l2, l3, b0, b1);
+                mma_f16(o[2 * np], a0, a1, a2, a3, c0, c1);
                 mma_f16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                mma_f16(o[2 * np + 1], l0, l1, l2, l3, b2, b3);
+                mma_f16(o[2 * np + 1], a0, a1, a2, a3, c2, c3);
             }
         }
-        __syncthreads();   // the buffer is refilled next iteration
+        __syncthreads();   // every warp is done with this tile's parts
+        if (t + 1 < ntiles) split_tile();
     }
     // ---- normalise and store the warp's rows
     const int m_a = q0 + r0 + gq, m_b = m_a + 8;
@@ -582,9 +617,8 @@ static bool pf_layer(const Plan *P, const Plan &h, const LayerW &w, KvT<T> *kc, 
     k_pf_rope_kv<KV><<<M, 256, 0, s>>>(P, h.pf_QKV, p0, kc, vc);
     if constexpr (TC) {
         const dim3 fg((M + FA_BQ - 1) / FA_BQ, h.Hq);
-        const __half *kh = reinterpret_cast<const __half *>(kc), *vh = reinterpret_cast<const __half *>(vc);
-        if (h.hd == 128) k_pf_fa<128><<<fg, FA_THREADS, fa_smem_bytes<128>(), s>>>(P, h.pf_QKV, p0, M, kh, vh, h.pf_ATT);
-        else k_pf_fa<64><<<fg, FA_THREADS, fa_smem_bytes<64>(), s>>>(P, h.pf_QKV, p0, M, kh, vh, h.pf_ATT);
+        if (h.hd == 128) k_pf_fa<128><<<fg, FA_THREADS, fa_smem_bytes<128>(), s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
+        else k_pf_fa<64><<<fg, FA_THREADS, fa_smem_bytes<64>(), s>>>(P, h.pf_QKV, p0, M, kc, vc, h.pf_ATT);
     } else {
         const int G = h.Hq / h.Hkv, QB = 64 / G;
         dim3 ag((M + QB - 1) / QB, h.Hkv);
@@ -663,7 +697,6 @@ void launch_rope_table(const Plan &h, float theta, cudaStream_t s) {
 
 void set_prefill_attributes() {
     cudaFuncSetAttribute(k_pf_attn<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
-    cudaFuncSetAttribute(k_pf_attn<KvT<__nv_bfloat16>, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * PF_KT * 128 * 4);
     cudaFuncSetAttribute(k_pf_logits<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     cudaFuncSetAttribute(k_pf_logits<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
     cudaFuncSetAttribute(k_pf_fa<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, fa_smem_bytes<128>());

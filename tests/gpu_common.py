@@ -42,7 +42,7 @@ class Case:
 
     @property
     def kv_dtype(self):
-        return np.float32 if self.dm.dtype == "fp32" else np.float16
+        return np.float32   # the library's K/V caches hold fp32 rows for every weight type
 
 
 _cache = {}
