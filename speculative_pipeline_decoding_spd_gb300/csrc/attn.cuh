@@ -29,7 +29,10 @@ constexpr int ATT_MAXHD = 128;
 constexpr int ATT_HB = 4;       // heads per weighted-sum pass
 // CTAs per SM the register budget is sized for: one wave for 8 stages x 8 kv heads of a
 // 2K-position context
-template <typename T> __host__ __device__ constexpr int att_min_blocks() { return sizeof(T) == 2 ? 3 : 1; }
+template <typename T> __host__ __device__ constexpr int att_min_blocks() { return sizeof(T) == 2 ? 3 : 2; }
+// fp32 rows: K and V of a chunk take turns in one buffer (the V rows are copied in once the
+// scores are done), so that two CTAs fit on an SM and one's copies overlap the other's work
+template <typename T> __host__ __device__ constexpr bool att_onebuf() { return sizeof(T) == 4; }
 
 // K and V rows live in shared memory as 32-bit words: 16-bit pairs (T = fp16 or bf16) or
 // floats.  lo / hi widen the first / second element of a pair.
@@ -63,12 +66,14 @@ __host__ __device__ constexpr int att_words(int hd) { return hd / KVW<T>::PER; }
 template <typename T>
 __host__ __device__ constexpr int att_pitch(int hd) { return att_words<T>(hd) + 4; }
 
-// dynamic shared memory (bytes): Ks [CHUNK][pitch] | Vs [CHUNK][pitch] words, then
-// qs [G][hd] and the scores [G][CHUNK] as floats.  After the scores the K rows hold the
-// per-warp weighted sums [8 warps][ATT_HB][hd] floats (16 KB at hd 128, below the K rows).
+// dynamic shared memory (bytes): Ks [CHUNK][pitch] | Vs [CHUNK][pitch] words (one buffer for
+// both with fp32 rows), then qs [G][hd] and the scores [G][CHUNK] as floats.  The per-warp
+// weighted sums [8 warps][ATT_HB][hd] floats (16 KB at hd 128) lie over the K rows after the
+// scores, or after the scores with fp32 rows (the V rows occupy the K rows there).
 template <typename T>
 __host__ __device__ constexpr int att_smem_bytes(int hd, int G) {
-    return 2 * ATT_CHUNK * att_pitch<T>(hd) * 4 + G * hd * 4 + G * ATT_CHUNK * 4;
+    return (att_onebuf<T>() ? 1 : 2) * ATT_CHUNK * att_pitch<T>(hd) * 4 + G * hd * 4 + G * ATT_CHUNK * 4 +
+           (att_onebuf<T>() ? (ATT_THREADS / 32) * ATT_HB * hd * 4 : 0);
 }
 
 // One attention problem: a single query token of Hq heads against cache positions
@@ -118,24 +123,22 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
     const long long rowstride = (long long)Hkv * hd;
     const bool owner = a.kraw != nullptr && (c == nch - 1);
     const int W = att_words<T>(hd), KP = att_pitch<T>(hd);
-    uint32_t *Ks = kv_smem, *Vs = kv_smem + ATT_CHUNK * KP;
-    float *qs = reinterpret_cast<float *>(Vs + ATT_CHUNK * KP);   // [G][hd]
+    constexpr bool ONEBUF = att_onebuf<T>();
+    uint32_t *Ks = kv_smem, *Vs = ONEBUF ? kv_smem : kv_smem + ATT_CHUNK * KP;
+    float *qs = reinterpret_cast<float *>(kv_smem + (ONEBUF ? 1 : 2) * ATT_CHUNK * KP);   // [G][hd]
     float *sc = qs + G * hd;                                       // [G][CHUNK]
-
-    // ---- this chunk's K and V rows of kv head g: asynchronous 16-byte copies
-    {
-        const int vpr = hd * (int)sizeof(T) / 16;   // 16-byte vectors per row
-        const int total = cnt * vpr;
-        const long long base = ((long long)j0 * rowstride + (long long)g * hd) * (long long)sizeof(T);
-        const char *kb = reinterpret_cast<const char *>(a.kc) + base;
-        const char *vb = reinterpret_cast<const char *>(a.vc) + base;
-        for (int idx = tid; idx < total; idx += ATT_THREADS) {
+    // ---- this chunk's K (and, two buffers, V) rows of kv head g: asynchronous 16-byte copies
+    const int vpr = hd * (int)sizeof(T) / 16;   // 16-byte vectors per row
+    const long long cbase = ((long long)j0 * rowstride + (long long)g * hd) * (long long)sizeof(T);
+    auto copy_rows = [&](uint32_t *dst, const T *src) {
+        const char *sb = reinterpret_cast<const char *>(src) + cbase;
+        for (int idx = tid; idx < cnt * vpr; idx += ATT_THREADS) {
             const int j = idx / vpr, q = idx - j * vpr;
-            const long long off = (long long)j * rowstride * (long long)sizeof(T) + 16 * q;
-            cp_async16(Ks + j * KP + 4 * q, kb + off);
-            cp_async16(Vs + j * KP + 4 * q, vb + off);
+            cp_async16(dst + j * KP + 4 * q, sb + (long long)j * rowstride * (long long)sizeof(T) + 16 * q);
         }
-    }
+    };
+    copy_rows(Ks, a.kc);
+    if (!ONEBUF) copy_rows(Vs, a.vc);
     // ---- the chunk's older positions come from earlier steps; q, k_new and v_new from the
     // preceding launch of this stream
     pdl_wait();
@@ -186,7 +189,7 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
                 Vs[j * KP + w] = KVW<T>::pack(vnew[2 * w], vnew[2 * w + 1]);
             } else {
                 Ks[j * KP + w] = __float_as_uint(knew[w]);
-                Vs[j * KP + w] = __float_as_uint(vnew[w]);
+                if (!ONEBUF) Vs[j * KP + w] = __float_as_uint(vnew[w]);
             }
         }
         __syncthreads();
@@ -236,6 +239,7 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
         }
     }
     __syncthreads();
+    if (ONEBUF) copy_rows(Vs, a.vc);   // every K row has been read: the V rows take their place
     // ---- chunk softmax per head
     for (int h = warp; h < G; h += ATT_THREADS / 32) {
         float *sh = sc + h * ATT_CHUNK;
@@ -254,6 +258,12 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
             s_l[h] = l;
         }
     }
+    if (ONEBUF) {
+        cp_async_wait_all();
+        __syncthreads();
+        if (owner)
+            for (int w = tid; w < W; w += ATT_THREADS) Vs[(pos - j0) * KP + w] = __float_as_uint(vnew[w]);
+    }
     __syncthreads();
     // ---- o = sum_j p_j v_j: thread = (16-byte vector vo of the row, position group qg),
     // positions qg, qg + NQ, ...; ATT_HB heads per pass
@@ -263,7 +273,7 @@ __device__ void attn_cta(const AttnArgs<T> &a, int g, int c) {
     constexpr int EPV = 16 / (int)sizeof(T);        // elements per vector
     const int LPR = hd / EPV, NQ = ATT_THREADS / LPR;
     const int vo = tid % LPR, qg = tid / LPR;
-    float *ored = reinterpret_cast<float *>(kv_smem);   // [8 warps][ATT_HB][hd], over the K rows
+    float *ored = ONEBUF ? sc + G * ATT_CHUNK : reinterpret_cast<float *>(kv_smem);   // [8 warps][ATT_HB][hd]
     for (int hb = 0; hb < G; hb += ATT_HB) {
         float o[ATT_HB][EPV];
 #pragma unroll
