@@ -9,8 +9,7 @@
 //   QKV fp32 [n][(Hq+2Hkv) hd]   raw q,k,v of each stage (RoPE is applied by the attention kernel)
 //   att_part fp32 [stage][Hq][chunk][hd+4]  attention chunk partials (merged by the O projection)
 //   U   fp32 [n][2F]             raw gate and up sums of each stage (SiLU(gate)*up formed by the down GEMV)
-//   K/V cache per target layer   [max_seq][Hkv][hd] in the KV type (fp16 for bf16 weights, fp32 for
-//                                fp32 weights); valid length per layer in DevState
+//   K/V cache per target layer   fp32 [max_seq][Hkv][hd]; valid length per layer in DevState
 //   draft module buffers         Xp [n+1][d], QKVp/ATTp/GUp per row, its own K/V cache
 //   logits fp32 [2][V]           row 0 = target prediction of the exiting token, row 1 = draft
 #pragma once
@@ -210,8 +209,8 @@ template <> struct WTraits<__nv_bfloat16> {
     __device__ static __forceinline__ float get(const __nv_bfloat16 *p, long long i) { return __bfloat162float(p[i]); }
     __device__ static __forceinline__ __nv_bfloat16 store(float v) { return __float2bfloat16_rn(v); }
 };
-// fp16: the KV cache of bf16 models (same bytes as bf16, three more mantissa bits).  Values
-// beyond the fp16 range saturate at +-65504 instead of becoming infinite.
+// fp16: a K/V operand type of the stand-alone attention call.  Values beyond the fp16 range
+// saturate at +-65504 instead of becoming infinite.
 constexpr float F16_MAX = 65504.f;
 template <> struct WTraits<__half> {
     static constexpr int VEC = 8;

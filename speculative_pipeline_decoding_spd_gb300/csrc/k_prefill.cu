@@ -9,7 +9,7 @@
 // GEMM (umma.cuh: tcgen05, TMEM accumulators, TMA-fed operands) whose activation operand
 // comes as two bf16 parts written by the kernel before it (the norm, the attention
 // output's split, SiLU(gate) * up, the anchors' split), and the causal attention runs on
-// tensor cores too (mma.sync over the fp16 K/V cache, flash-attention order).  fp32
+// tensor cores too (mma.sync, flash-attention order, the fp32 K/V rows split into fp16 parts).  fp32
 // weights: an fp32 tiled CUDA-core GEMM and attention.
 #include <cudaTypedefs.h>
 

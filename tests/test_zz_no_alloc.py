@@ -54,7 +54,7 @@ def _no_alloc(q, k, v, dtype):
 def test_no_alloc_matches_caller_scratch_on_two_calls_in_a_row():
     # several chunks each, so the arrival counters and the partials are both used; every
     # call after the first runs on other data right after the one before left its scratch
-    # behind; the KV types of the library (fp16, fp32) and bf16; the largest sequence that
+    # behind; the K/V operand types of the call (fp32, bf16, fp16); the largest sequence that
     # fits the built-in buffer at Hq 32, hd 128 (7936 positions, 62 chunks)
     cases = [(32, 8, 128, 1000, 11, B.SPD_BF16), (16, 2, 128, 700, 12, B.SPD_BF16),
              (32, 8, 128, 900, 14, B.SPD_F32), (8, 4, 64, 333, 15, B.SPD_F16), (32, 8, 128, 7936, 16, B.SPD_F16)]
