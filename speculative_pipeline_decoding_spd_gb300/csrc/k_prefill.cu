@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(256) k_pf_attn(const Plan *__restrict__ P, con
 
 // ---- causal attention of a prompt chunk on tensor cores (fp32 K/V cache) ------------------
 // CTA = 64 query rows of one query head (4 warps x 16 rows), flash-attention order over key
-// tiles of 64 positions.  cp.async copies the next tile's fp32 K and V rows into a staging
+// tiles of 32 positions.  cp.async copies the next tile's fp32 K and V rows into a staging
 // buffer while the warps work on the current tile, which has been split into fp16 parts
 // hi = fp16(x) and lo = fp16(x - hi) (about 21 bits of each value).  Scores S = Q K^T by
 // mma.sync m16n8k16 as q_hi k_hi + q_lo k_hi + q_hi k_lo (q pre-scaled by 1/sqrt(hd) and split
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(256) k_pf_attn(const Plan *__restrict__ P, con
 // softmax per row in registers, the probabilities split the same way and
 // O += P_hi V_hi + P_lo V_hi + P_hi V_lo; the causal mask applies on the diagonal tile only.
 // Output fp32 [row][Hq * hd], as the tensor-core O projection's input split expects.
-constexpr int FA_BQ = 64, FA_BK = 64, FA_THREADS = 128;
+constexpr int FA_BQ = 64, FA_BK = 32, FA_THREADS = 128;   // 32-key tiles: two CTAs per SM
 template <int HD> __host__ __device__ constexpr int fa_pitch() { return HD + 8; }   // halfs; ldmatrix rows on distinct banks
 template <int HD> __host__ __device__ constexpr int fa_smem_bytes() {
     // q hi / lo, K hi / lo, V hi / lo (fp16 tiles), then the fp32 K and V staging rows
