@@ -58,3 +58,9 @@ def test_workload_selection():
     A.mode, A.shape, A.n = "forced-0.7", "8b", 16
     wl = bench.select_workload(A)
     assert wl.dims == si.SHAPE_8B.dims and wl.n == 16 and wl.prompt_len == 4096 and wl.Ls == 2
+
+
+def test_l2_note_follows_the_bytes_streamed_per_step():
+    # the 4B workload streams gigabytes per step: no flush; the tiny fp32 model sits in L2
+    assert bench.l2_note(6.1e9).startswith("no flush needed")
+    assert bench.l2_note(23e6).startswith("L2-resident")
