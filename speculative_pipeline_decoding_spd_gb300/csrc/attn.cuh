@@ -6,7 +6,8 @@
 // reads a few MB of K/V spread over hundreds of CTAs), so every global access is issued
 // as early as possible and all of a thread's loads are in flight together:
 //   * the chunk's K and V rows go to shared memory by asynchronous 16-byte copies (no
-//     registers held while they are in flight), q is staged (and rotated) meanwhile;
+//     registers held while they are in flight), q is staged (and rotated) meanwhile; fp32
+//     rows (the pipeline's caches) share one buffer: K first, V once the scores are done;
 //   * scores: thread = (position, head parity), 16-byte K reads from a row pitch that
 //     puts 8 consecutive rows on distinct banks, q broadcast from shared memory;
 //   * softmax per head in one warp, then o = sum_j p_j v_j with thread = (16-byte vector
