@@ -74,3 +74,20 @@ def test_no_alloc_refuses_shapes_beyond_its_buffer():
                                            q.data_ptr(), 0)
         assert e.value.code == B.SPD_ECAPACITY
         assert "scratch" in B.spd_ops_last_error()
+
+
+def test_no_alloc_replays_inside_a_cuda_graph():
+    # the first call (outside any capture) looks up the array's device address; a second call
+    # captured into a graph and replayed gives what the caller-scratch entry point gives
+    q, k, v, dt = _inputs(32, 8, 128, 1000, 17)
+    ref = _with_scratch(q, k, v, dt)
+    _no_alloc(q, k, v, dt)
+    out = torch.zeros(32, 128, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        B.spd_attention_decode_noalloc(dt, 32, 8, 128, 1000, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                       out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    graph.replay()
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= TOL
